@@ -1,0 +1,329 @@
+"""CPU oracle for the forward pass of a top-k Mixture-of-Experts FFN layer.
+
+TEST INFRASTRUCTURE.  Only the tests, `__graft_entry__.smoke()` and the CPU-baseline /
+reference legs of `bench.py` may import or run this module.  It shares no code with the
+CUDA library (it imports nothing from the product package), and the library never imports
+it.  Inputs come from the seeded generator in `workloads/`, which both sides use.
+
+It is a plain, slow, obviously-correct restatement of the layer as the pages define it:
+
+    MoE(x) = f_shared(x) + sum_{e in TopK(x)} g_e(x) f_e(x)
+    f_e(x) = ((x W1_e) * Swish(x W2_e)) W3_e,   Swish = SiLU (beta = 1)
+
+Sources (page title, section):
+  [MM]  "8.6 - Mixture of Experts (MoE)": section 2 (SwiGLU expert, router x W_g, top-k by
+        largest logit, gates exp(l_e) / sum over the chosen k, layer output), section 2.1
+        (FLOP and parameter counts), section 3.1 (auxiliary loss), section 3.2 (capacity),
+        section 4 (combinations), section 4.1 (shared expert).
+  [FM]  "Mixture-of-Experts Internals: A Systems Engineer's Field Manual": section 2.1
+        (softmax over all E, top-k, renormalise over the chosen k), section 3.3 (bias used
+        only for selection), section 4.2 (dispatch volume).
+  [RA]  "Mixture-of-Experts, from the router to the all-to-all": "The router" (sigmoid
+        scores normalised over the chosen k), "Experts, fine-grained and shared" (P_e =
+        3 d d_ff, combination counts), "Why total and active parameters come apart",
+        "Capacity and token dropping".
+  [TR]  "Mixture of Experts: What Actually Happens When a Token Hits the Router": Step 3
+        (the masked per-expert loop; sort by expert, one matmul per expert, scatter back),
+        Step 4 (down(silu(gate(x)) * up(x)), weighted sum).
+
+Precision.  The router logits are formed in float64 from the stored (float32 or bfloat16)
+values and rounded once to float32: the top-k decision is taken on float32 values on both
+sides, as the pages keep the router in float32.  Biases are added in float32.  Scores,
+gates, the experts and the combine are float64.
+
+Pins (tests/test_oracle_pins.py): every function here is checked against something other
+than itself: closed forms, printed values, special cases that reduce to a dense SwiGLU FFN
+or a full softmax, brute force over all k-subsets, and an independent per-token evaluation.
+The numeric values of y for the five synthetic workloads are not printed by the pages; they
+are trusted through those pins.
+"""
+from __future__ import annotations
+
+import math
+from typing import Callable, Dict, Optional, Sequence
+
+import numpy as np
+
+from workloads import to_f64
+
+# --------------------------------------------------------------------------------------
+# Router: logits, scores, top-k, gates
+# --------------------------------------------------------------------------------------
+
+
+def router_logits(x64: np.ndarray, Wg64: np.ndarray,
+                  logit_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """Router logits l = x W_g (+ bias), as float32 [T, E].
+
+    [MM] section 2: router(x) = x W_g with W_g of shape d x E.  [FM] section 2.1 writes the
+    same map as W_r x with W_r = W_g^T.  The per-expert bias of the skewed workload is added
+    to the logits, so it shifts both the scores and the selection."""
+    l = (np.asarray(x64, np.float64) @ np.asarray(Wg64, np.float64)).astype(np.float32)
+    if logit_bias is not None:
+        l = (l + np.asarray(logit_bias, np.float32)).astype(np.float32)
+    return l
+
+
+def scores(l32: np.ndarray, scoring: str) -> np.ndarray:
+    """Per-expert scores in float64.
+
+    softmax: s = softmax(l) over all E experts ([FM] section 2.1; [RA] "The router").
+    sigmoid: s_e = 1 / (1 + exp(-l_e)), DeepSeek-V3's scoring ([RA] "The router")."""
+    l = np.asarray(l32, np.float64)
+    if scoring == "softmax":
+        m = l.max(axis=-1, keepdims=True)
+        e = np.exp(l - m)
+        return e / e.sum(axis=-1, keepdims=True)
+    if scoring == "sigmoid":
+        return 1.0 / (1.0 + np.exp(-l))
+    raise ValueError(scoring)
+
+
+def select_topk(key32: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest keys per row, in descending key order; equal keys go to the
+    lower expert id.  [MM] section 2: the k experts with the largest gate logits."""
+    key = np.asarray(key32, np.float32)
+    order = np.argsort(-key, axis=-1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def gates_from_scores(s64: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """g_j = s_{I_j} / sum_{j'} s_{I_j'}: the chosen scores renormalised to sum to 1.
+
+    [FM] section 2.1 (renormalised gates; zero outside the chosen set) and [RA] "The router"
+    (sigmoid scores normalised among the selected)."""
+    sel = np.take_along_axis(np.asarray(s64, np.float64), idx.astype(np.int64), axis=-1)
+    return sel / sel.sum(axis=-1, keepdims=True)
+
+
+def route(x64: np.ndarray, Wg64: np.ndarray, k: int, scoring: str,
+          logit_bias: Optional[np.ndarray] = None,
+          sel_bias: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Router logits -> scores -> top-k -> gates for every token.
+
+    Selection runs on l (+ sel_bias, a bias used for choosing only, [FM] section 3.3; the
+    gates come from the unbiased scores).  Returns idx [T, k] int32, gate [T, k] float64,
+    logits [T, E] float32."""
+    l = router_logits(x64, Wg64, logit_bias)
+    key = l if sel_bias is None else (l + np.asarray(sel_bias, np.float32)).astype(np.float32)
+    idx = select_topk(key, k)
+    g = gates_from_scores(scores(l, scoring), idx)
+    return {"idx": idx, "gate": g, "logits": l}
+
+
+# --------------------------------------------------------------------------------------
+# Dispatch: histogram, offsets, permutation
+# --------------------------------------------------------------------------------------
+
+
+def dispatch(idx: np.ndarray, E: int) -> Dict[str, np.ndarray]:
+    """Group the (token, slot) pairs by expert ([TR] Step 3: sort tokens by assigned expert
+    into contiguous blocks).
+
+    counts[e]   = number of pairs routed to expert e
+    offsets[e]  = sum of counts before e; offsets[E] = T k
+    perm_tok[p] = token of the p-th pair in expert order (pairs of one expert keep the order
+                  of their flattened index t k + j)
+    inv_pos[t, j] = position p of pair (t, j)."""
+    T, k = idx.shape
+    flat = idx.reshape(-1).astype(np.int64)
+    counts = np.bincount(flat, minlength=E).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    order = np.argsort(flat, kind="stable")
+    perm_tok = (order // k).astype(np.int32)
+    inv = np.empty(T * k, dtype=np.int32)
+    inv[order] = np.arange(T * k, dtype=np.int32)
+    return {"counts": counts, "offsets": offsets, "perm_tok": perm_tok,
+            "inv_pos": inv.reshape(T, k)}
+
+
+# --------------------------------------------------------------------------------------
+# Experts
+# --------------------------------------------------------------------------------------
+
+
+def silu(v: np.ndarray) -> np.ndarray:
+    """Swish with beta = 1 (SiLU): v * sigmoid(v)."""
+    return v / (1.0 + np.exp(-v))
+
+
+def swiglu_expert(X64: np.ndarray, W1: np.ndarray, W2: np.ndarray, W3: np.ndarray) -> np.ndarray:
+    """f(x) = ((x W1) * Swish(x W2)) W3 for every row of X, in float64 ([MM] section 2).
+    W2 is the gated projection ([TR] Step 4 writes down(silu(gate(x)) * up(x)))."""
+    u = X64 @ W1
+    v = X64 @ W2
+    return (u * silu(v)) @ W3
+
+
+WeightFn = Callable[[str, int], np.ndarray]   # (name, expert) -> float64 matrix
+
+
+def weights_from_arrays(arrays: Dict[str, np.ndarray], dtype: str) -> WeightFn:
+    """Adapter: stacked stored arrays {"W1": [E, d, d_ff], ...} -> float64 per expert."""
+    def get(name: str, e: int) -> np.ndarray:
+        return to_f64(arrays[name][e], dtype)
+    return get
+
+
+def experts_grouped(x_perm64: np.ndarray, offsets: np.ndarray, get_w: WeightFn) -> np.ndarray:
+    """Each expert e runs once on its contiguous block rows offsets[e]:offsets[e+1] of the
+    permuted activations ([TR] Step 3, one dense matmul per expert).  Empty experts are
+    skipped.  Returns y_perm [T k, d] float64."""
+    E = len(offsets) - 1
+    y = np.zeros((x_perm64.shape[0], get_w("W3", 0).shape[1] if E else 0), np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            y[a:b] = swiglu_expert(x_perm64[a:b], get_w("W1", e), get_w("W2", e), get_w("W3", e))
+    return y
+
+
+def shared_experts(x64: np.ndarray, get_w: WeightFn, n_shared: int) -> Optional[np.ndarray]:
+    """Sum of the always-on shared experts, gate 1 ([MM] section 4.1; [FM] section 6.2)."""
+    if n_shared <= 0:
+        return None
+    ys = np.zeros((x64.shape[0], x64.shape[1]), np.float64)
+    for s in range(n_shared):
+        ys += swiglu_expert(x64, get_w("Ws1", s), get_w("Ws2", s), get_w("Ws3", s))
+    return ys
+
+
+def combine(y_perm64: np.ndarray, inv_pos: np.ndarray, gate64: np.ndarray,
+            shared64: Optional[np.ndarray] = None) -> np.ndarray:
+    """y[t] = sum_j g[t, j] y_perm[inv_pos[t, j]] (+ shared[t]): scatter the expert outputs
+    back to token order and weight them by the gates ([MM] section 2; [TR] Step 3/4)."""
+    T, k = inv_pos.shape
+    y = np.zeros((T, y_perm64.shape[1]), np.float64)
+    for j in range(k):
+        y += gate64[:, j:j + 1] * y_perm64[inv_pos[:, j]]
+    if shared64 is not None:
+        y += shared64
+    return y
+
+
+def forward(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, k: int,
+            scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0) -> Dict[str, np.ndarray]:
+    """The whole layer, evaluated the grouped way: route, dispatch, one SwiGLU per expert
+    over its block, combine (+ shared experts).  All results are returned for comparison."""
+    r = route(x64, Wg64, k, scoring, logit_bias, sel_bias)
+    dsp = dispatch(r["idx"], E)
+    x_perm = x64[dsp["perm_tok"]]
+    y_perm = experts_grouped(x_perm, dsp["offsets"], get_w)
+    ys = shared_experts(x64, get_w, n_shared)
+    y = combine(y_perm, dsp["inv_pos"], r["gate"], ys)
+    out = dict(r)
+    out.update(dsp)
+    out.update({"y_perm": y_perm, "y": y, "y_shared": ys})
+    return out
+
+
+def forward_tokens(x_rows64: np.ndarray, idx_rows: np.ndarray, gate_rows: np.ndarray,
+                   get_w: WeightFn, n_shared: int = 0) -> np.ndarray:
+    """The layer output for a few tokens, given their routing, by the definition
+    MoE(x) = sum_j g_j f_{I_j}(x) (+ shared): each chosen expert evaluated on the token
+    itself ([MM] section 2).  Tokens that share an expert are evaluated together."""
+    n, k = idx_rows.shape
+    y = np.zeros((n, x_rows64.shape[1]), np.float64)
+    for e in np.unique(idx_rows):
+        rows, slots = np.nonzero(idx_rows == e)
+        fe = swiglu_expert(x_rows64[rows], get_w("W1", int(e)), get_w("W2", int(e)), get_w("W3", int(e)))
+        y[rows] += gate_rows[rows, slots][:, None] * fe
+    ys = shared_experts(x_rows64, get_w, n_shared)
+    return y if ys is None else y + ys
+
+
+def forward_bruteforce(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, k: int,
+                       scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0) -> np.ndarray:
+    """The naive evaluation ([TR] Step 3): loop over experts, mask the tokens that chose
+    each, run the expert on them, weight by the gate and accumulate.  No sort, no offsets,
+    no permutation: an independent evaluation of the same sum, for tiny inputs."""
+    r = route(x64, Wg64, k, scoring, logit_bias, sel_bias)
+    T = x64.shape[0]
+    y = np.zeros_like(x64, dtype=np.float64)
+    for e in range(E):
+        for t in range(T):
+            for j in range(k):
+                if r["idx"][t, j] == e:
+                    f = swiglu_expert(x64[t:t + 1], get_w("W1", e), get_w("W2", e), get_w("W3", e))[0]
+                    y[t] += r["gate"][t, j] * f
+    ys = shared_experts(x64, get_w, n_shared)
+    return y if ys is None else y + ys
+
+
+# --------------------------------------------------------------------------------------
+# Counting helpers (printed quantities on the pages)
+# --------------------------------------------------------------------------------------
+
+
+def n_combinations(E: int, k: int) -> int:
+    """Number of distinct k-expert sets out of E: E! / (k! (E-k)!), in exact integers
+    ([MM] section 4; [RA] "Experts, fine-grained and shared")."""
+    if k < 0 or k > E:
+        return 0
+    num, den = 1, 1
+    for i in range(k):
+        num *= E - i
+        den *= i + 1
+    return num // den
+
+
+def expert_params(d: int, d_ff: int) -> int:
+    """Weights of one SwiGLU expert: P_e = 3 d d_ff ([RA] "Experts, fine-grained and shared")."""
+    return 3 * d * d_ff
+
+
+def moe_ffn_params(E: int, d: int, d_ff: int) -> int:
+    """Weights of one MoE FFN sub-layer: E (3 d d_ff) + d E ([MM] section 2.1)."""
+    return E * expert_params(d, d_ff) + d * E
+
+
+def total_active_params(N0: int, L: int, E: int, k: int, P_e: int):
+    """(N_total, N_active) = (N0 + L E P_e, N0 + L k P_e)
+    ([RA] "Why total and active parameters come apart")."""
+    return N0 + L * E * P_e, N0 + L * k * P_e
+
+
+def flops_per_token(d: int, d_ff: int, E: int, k: int, n_shared: int = 0, d_ff_shared: int = 0) -> int:
+    """Forward FLOPs per token: router 2 d E plus 6 d d_ff per evaluated SwiGLU expert
+    (two d x d_ff and one d_ff x d matrix-vector product; [MM] section 2.1 gives 16 d^2 k
+    when d_ff = 8d/3)."""
+    return 2 * d * E + 6 * d * d_ff * k + 6 * d * d_ff_shared * n_shared
+
+
+def p_expert_unused(E: int, k: int, batch: int) -> float:
+    """Chance that one expert is chosen by none of `batch` tokens that each pick k of E
+    uniformly: ((E - k) / E)^batch ([RA] "Why total and active parameters come apart")."""
+    return ((E - k) / E) ** batch
+
+
+def capacity(tokens: int, E: int, k: int, factor: float) -> float:
+    """Expert capacity tokens k / E * factor ([MM] section 3.2; [RA] "Capacity and token
+    dropping")."""
+    return tokens * k / E * factor
+
+
+def dropped(picks: int, cap: int) -> int:
+    """Assignments an expert drops when picked more often than its capacity allows."""
+    return max(0, picks - cap)
+
+
+def aux_loss(f: np.ndarray, P: np.ndarray, alpha: float) -> float:
+    """Switch load-balancing loss alpha E sum_i f_i P_i ([MM] section 3.1; [FM] section 3.2)."""
+    f = np.asarray(f, np.float64)
+    P = np.asarray(P, np.float64)
+    return float(alpha * len(f) * np.sum(f * P))
+
+
+def dispatch_bytes(T: int, k: int, d: int, elem_bytes: int) -> int:
+    """Bytes of one dispatch exchange: T k d elements ([FM] section 4.2)."""
+    return T * k * d * elem_bytes
+
+
+def min_adjacent_gap(key32: np.ndarray, m: int) -> np.ndarray:
+    """Per row, the smallest difference between consecutive keys among the m largest (ranks
+    1..m in descending order).  Used to redraw tokens whose top-k could flip on rounding."""
+    key = np.asarray(key32, np.float32).astype(np.float64)
+    srt = -np.sort(-key, axis=-1)[:, :m]
+    if m < 2:
+        return np.full(key.shape[0], np.inf)
+    return np.min(srt[:, :-1] - srt[:, 1:], axis=-1)
