@@ -1,0 +1,207 @@
+/*
+ * moe.h - C ABI of libmoe, the forward pass of a top-k Mixture-of-Experts FFN layer on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The layer (page "8.6 - Mixture of Experts (MoE)", section 2, and section 4.1 for the
+ * shared expert):
+ *
+ *     l      = x W_g (+ logit_bias)                          router logits, float32
+ *     s      = softmax(l) over all E   |  sigmoid(l)         scores
+ *     I      = the k experts with the largest l (+ sel_bias)  top-k, descending
+ *     g_j    = s_{I_j} / sum_{j'} s_{I_j'}                    gates over the chosen k
+ *     f_e(x) = ((x W1_e) * SiLU(x W2_e)) W3_e                 SwiGLU expert
+ *     y      = sum_j g_j f_{I_j}(x) + sum_s f_shared_s(x)
+ *
+ * The calls follow the pages' four moves of one MoE layer - route, dispatch, compute,
+ * combine (page "Mixture-of-Experts, from the router to the all-to-all", section "Expert
+ * parallelism and the all-to-all"; page "Mixture of Experts: What Actually Happens When a
+ * Token Hits the Router", Step 3: sort tokens by expert into contiguous blocks, one matmul
+ * per expert, scatter back) - and moe_forward chains them.
+ *
+ * Conventions for every call
+ *  - Pointers named x, W_g, W1, W2, W3, Ws1, Ws2, Ws3, y, x_perm, y_perm, topk_*, counts,
+ *    offsets, perm_tok, inv_pos, logit_bias, sel_bias and ws are DEVICE pointers on the
+ *    current CUDA device; `cfg` is a host pointer.  The caller owns all memory.  The
+ *    library allocates and frees nothing; scratch comes from the caller's workspace `ws`
+ *    of `ws_bytes` bytes (moe_workspace_bytes gives a size that is enough for any call).
+ *  - All arrays are dense and row-major.  dtype (cfg->dtype) applies to x, W_g, the expert
+ *    weights, x_perm and y.  Biases, gates, logits, y_perm and all accumulation are float32.
+ *    Weights use the pages' x W orientation: W1, W2 are [E][d][d_ff], W3 is [E][d_ff][d],
+ *    W_g is [d][E]; shared weights Ws1, Ws2 are [n_shared][d][d_ff_shared], Ws3 is
+ *    [n_shared][d_ff_shared][d].
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and never synchronise, except moe_get_device_error and moe_forward_host.
+ *    Calls on different streams need distinct workspaces.
+ *  - Errors: every call returns a moe_status and never aborts.  The configuration and
+ *    pointers are checked on the host before anything is launched (MOE_ERR_INVALID_ARG,
+ *    MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE); a failed launch gives MOE_ERR_CUDA.
+ *    Conditions that only the device can see (an expert id out of range in moe_dispatch's
+ *    input, a pipeline wait that timed out) set a device error word that
+ *    moe_get_device_error reports.
+ *  - T = 0 is valid: the calls launch nothing and return MOE_OK.
+ *
+ * Limits: 1 <= k <= min(E, 32), E <= 1024, d, d_ff >= 1.  For bfloat16, d, d_ff, E (when
+ * E > 32) and d_ff_shared must be multiples of 8 and every pointer 16-byte aligned
+ * (the tensor-core path reads them through TMA).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;   /* same handle as cudaEvent_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad sizes, k > E, null required pointer, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2, /* valid MoE, but outside the shapes this library implements */
+  MOE_ERR_WORKSPACE = 3,   /* ws is NULL or ws_bytes is too small for this call */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_DEVICE = 5       /* the device flagged an error (see moe_get_device_error) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  /* softmax over all E, top-k, renormalise over the chosen k (page "Mixture-of-Experts
+     Internals: A Systems Engineer's Field Manual", section 2.1) */
+  MOE_SOFTMAX_TOPK_RENORM = 0,
+  /* sigmoid per expert, top-k, normalise among the chosen k (page "Mixture-of-Experts,
+     from the router to the all-to-all", section "The router", DeepSeek-V3) */
+  MOE_SIGMOID_TOPK_NORM = 1
+} moe_scoring;
+
+typedef struct {
+  int32_t T;           /* tokens */
+  int32_t d;           /* model width */
+  int32_t d_ff;        /* routed expert width */
+  int32_t E;           /* routed experts */
+  int32_t k;           /* experts chosen per token */
+  int32_t dtype;       /* moe_dtype */
+  int32_t scoring;     /* moe_scoring */
+  int32_t n_shared;    /* always-on shared experts (0 = none) */
+  int32_t d_ff_shared; /* shared expert width */
+} moe_config;
+
+/* Stages recorded by moe_forward_profiled: route, dispatch, experts (W1/W2 + SwiGLU),
+   experts (W3), shared experts, combine. */
+#define MOE_NUM_STAGES 6
+
+/* Workspace size in bytes that is enough for every call below with this configuration
+   (including moe_forward_host's device copies of x and y).  0 for an invalid config. */
+size_t moe_workspace_bytes(const moe_config* cfg);
+
+/* Route: logits -> scores -> top-k -> gates, for each token.
+   Page "8.6 - Mixture of Experts (MoE)", section 2 (router x W_g, top-k by largest logit,
+   gates normalised over the chosen k); page "Mixture-of-Experts Internals: A Systems
+   Engineer's Field Manual", sections 2.1 (softmax, top-k, renormalise) and 3.3 (bias used
+   for selection only); page "Mixture-of-Experts, from the router to the all-to-all",
+   section "The router" (sigmoid variant).
+     x          [T][d] dtype            W_g [d][E] dtype
+     logit_bias [E] float32 or NULL: added to the logits (enters scores and selection)
+     sel_bias   [E] float32 or NULL: added to the selection key only; gates stay unbiased
+     topk_idx   [T][k] int32 out: chosen experts in descending key order, ties -> lower id
+     topk_gate  [T][k] float32 out
+   ws: needs T*E*4 bytes (+ alignment) when E > 32, else may be NULL. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g,
+                     const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
+                     float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch: per-expert histogram, exclusive prefix sum, stable permutation, row gather.
+   Page "Mixture of Experts: What Actually Happens When a Token Hits the Router", Step 3
+   (sort tokens by assigned expert into contiguous blocks); page "T2.6 What MoE changes",
+   "Routing creates an assignment problem" (per-expert assignment counts).
+     topk_idx [T][k] int32 in (every id in [0, E); an id out of range sets the device
+              error word and that pair is skipped)
+     x        [T][d] dtype in
+     counts   [E] int32 out: pairs (t, j) routed to each expert
+     offsets  [E+1] int32 out: exclusive prefix sum of counts; offsets[E] = T*k
+     perm_tok [T*k] int32 out: token of the p-th pair in expert order; pairs of one
+              expert keep ascending flattened index t*k + j
+     inv_pos  [T][k] int32 out: position p of pair (t, j)
+     x_perm   [T*k][d] dtype out: x_perm[p] = x[perm_tok[p]]
+   Deterministic: no atomics; identical inputs give identical outputs. */
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                        int32_t* counts, int32_t* offsets, int32_t* perm_tok,
+                        int32_t* inv_pos, void* x_perm, void* ws, size_t ws_bytes,
+                        moe_stream_t stream);
+
+/* Experts: for each expert e, over its block rows offsets[e]..offsets[e+1] of x_perm,
+   y_perm = ((X W1_e) * SiLU(X W2_e)) W3_e.  Page "8.6 - Mixture of Experts (MoE)",
+   section 2 (SwiGLU expert); page "Mixture-of-Experts, from the router to the all-to-all",
+   section "Expert parallelism and the all-to-all" (one grouped matrix multiply per expert).
+     x_perm  [T*k][d] dtype   offsets [E+1] int32 (non-decreasing, offsets[0] = 0,
+             offsets[E] = T*k; as written by moe_dispatch)
+     W1, W2  [E][d][d_ff] dtype     W3 [E][d_ff][d] dtype
+     y_perm  [T*k][d] float32 out
+   The intermediate h = (X W1) * SiLU(X W2) is kept in ws in dtype (bfloat16 for the
+   bfloat16 path). Experts with no rows are skipped and their weights are not read. */
+moe_status moe_experts(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                       const void* W1, const void* W2, const void* W3, float* y_perm,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: y[t] = sum_{j<k} topk_gate[t][j] * y_perm[inv_pos[t][j]] + sum_s f_shared_s(x[t]),
+   summed in float32 in slot order j = 0..k-1 and rounded once to dtype.
+   Page "8.6 - Mixture of Experts (MoE)", sections 2 (gate-weighted sum) and 4.1 (shared
+   expert, gate 1); page "Mixture of Experts: What Actually Happens When a Token Hits the
+   Router", Step 3 (scatter back).
+     y_perm [T*k][d] float32   inv_pos [T][k] int32   topk_gate [T][k] float32
+     x [T][d] dtype, Ws1/Ws2/Ws3 as above: read only when cfg->n_shared > 0 (else may be NULL)
+     y [T][d] dtype out */
+moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* inv_pos,
+                       const float* topk_gate, const void* x, const void* Ws1,
+                       const void* Ws2, const void* Ws3, void* y, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* The whole layer: route -> dispatch -> experts -> combine (+ shared experts), on one
+   stream, with every intermediate in ws.  Page "8.6 - Mixture of Experts (MoE)", section 2
+   (MoE(x) = sum over TopK of g_e(x) f_e(x)) and section 4.1 (plus f_shared(x)).
+   topk_idx_out [T][k] int32 and counts_out [E] int32 are optional copies of the routing. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g,
+                       const float* logit_bias, const float* sel_bias, const void* W1,
+                       const void* W2, const void* W3, const void* Ws1, const void* Ws2,
+                       const void* Ws3, void* y, int32_t* topk_idx_out, int32_t* counts_out,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_forward that also records events[0..MOE_NUM_STAGES] on `stream` at the stage
+   boundaries (route | dispatch | W1/W2 | W3 | shared | combine); events[i+1] - events[i]
+   is stage i's device time (0 for a stage with no work).  `events` is a host array of
+   MOE_NUM_STAGES + 1 events created by the caller; NULL entries are skipped. */
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const void* W_g,
+                                const float* logit_bias, const float* sel_bias,
+                                const void* W1, const void* W2, const void* W3,
+                                const void* Ws1, const void* Ws2, const void* Ws3, void* y,
+                                int32_t* topk_idx_out, int32_t* counts_out, void* ws,
+                                size_t ws_bytes, moe_stream_t stream, moe_event_t* events);
+
+/* moe_forward with x and y in HOST memory (pinned memory gives the fastest copies):
+   copies x_host to the device, runs the layer and copies y back into y_host, all on
+   `stream`, then waits for the stream.  Weights, biases and ws are device pointers. */
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g,
+                            const float* logit_bias, const float* sel_bias, const void* W1,
+                            const void* W2, const void* W3, const void* Ws1, const void* Ws2,
+                            const void* Ws3, void* y_host, void* ws, size_t ws_bytes,
+                            moe_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the device error word of the current device.
+   Returns MOE_OK, MOE_ERR_DEVICE (and the raw word in *word when word != NULL), or
+   MOE_ERR_CUDA when the wait itself failed. */
+moe_status moe_get_device_error(moe_stream_t stream, uint32_t* word);
+
+/* Number of kernels the last call on this host thread launched. */
+int32_t moe_last_launch_count(void);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,222 @@
+// Dispatch of the MoE layer: per-expert histogram, exclusive prefix sum, stable permutation
+// and row gather (page "Mixture of Experts: What Actually Happens When a Token Hits the
+// Router", Step 3: sort tokens by assigned expert into contiguous blocks per expert).
+//
+// The T*k (token, slot) pairs, in flattened order i = t*k + j, are cut into chunks of 256
+// pairs, one chunk per warp.  No atomics anywhere, so counts, offsets and the permutation are
+// identical from run to run:
+//   hist     each warp counts its chunk per expert: __match_any_sync groups the lanes that
+//            hold the same expert, and the lowest such lane adds the group size to the
+//            warp's private histogram in shared memory.
+//   scan     one block: per-expert totals, exclusive scan over experts (offsets), and each
+//            chunk's starting position per expert (offsets[e] + pairs of e in earlier chunks).
+//   permute  each warp replays its chunk: a pair's position is its chunk's running position
+//            for that expert plus its rank among the lanes of the same expert in that round.
+//            Pairs of one expert therefore keep ascending i.
+//   gather   x_perm[p] = x[perm_tok[p]], one warp per row with 16-byte vector copies.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+extern thread_local int g_launches;
+
+namespace {
+
+constexpr int CHUNK = 256;     // pairs per warp
+constexpr int WARPS = 8;       // warps per block in hist / permute
+constexpr unsigned FULL = 0xffffffffu;
+
+__global__ void __launch_bounds__(WARPS * 32) hist_kernel(const int32_t* __restrict__ idx, long long N, int E,
+                                                          int n_chunks, int32_t* __restrict__ chunk_counts,
+                                                          uint32_t* err) {
+  extern __shared__ int sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * WARPS + warp;
+  int* h = sh + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (chunk >= n_chunks) return;
+  const long long base = (long long)chunk * CHUNK;
+  bool bad = false;
+  for (int r = 0; r < CHUNK / 32; ++r) {
+    const long long i = base + r * 32 + lane;
+    int e = -1;
+    if (i < N) {
+      e = __ldg(idx + i);
+      if (e < 0 || e >= E) { bad = true; e = -1; }
+    }
+    const unsigned m = __match_any_sync(FULL, e);
+    if (e >= 0 && lane == __ffs(m) - 1) h[e] += __popc(m);
+    __syncwarp();
+  }
+  if (bad) flag_error(err, ERR_EXPERT_ID);
+  for (int e = lane; e < E; e += 32) chunk_counts[(size_t)chunk * E + e] = h[e];
+}
+
+// One block of 1024 threads.  Thread (e, s) owns expert e's column of the [n_chunks][E]
+// count matrix over the chunk segment s (S segments per expert).
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts, int n_chunks, int E,
+                                                    int S, int32_t* __restrict__ chunk_base,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int part[1024];   // [S][E] segment sums, then exclusive segment bases
+  __shared__ int tot[1024];    // per-expert totals, then offsets
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x;
+  const int e = tid % E, s = tid / E;
+  const int seg = (n_chunks + S - 1) / S;
+  const bool active = tid < E * S;
+  const int c0 = s * seg, c1 = min(n_chunks, c0 + seg);
+  if (active) {
+    int acc = 0;
+    for (int c = c0; c < c1; ++c) acc += chunk_counts[(size_t)c * E + e];
+    part[s * E + e] = acc;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+    for (int q = 0; q < S; ++q) {
+      const int v = part[q * E + tid];
+      part[q * E + tid] = run;
+      run += v;
+    }
+    tot[tid] = run;
+    counts[tid] = run;
+  }
+  __syncthreads();
+  // exclusive scan of tot[0..E) (E <= 1024) across the block
+  const int lane = tid & 31, w = tid >> 5;
+  int v = tid < E ? tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = wsum[lane];
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(FULL, xi, o);
+      if (lane >= o) xi += n;
+    }
+    wsum[lane] = xi - x;
+  }
+  __syncthreads();
+  const int excl = incl - v + wsum[w];
+  __syncthreads();
+  if (tid < E) {
+    tot[tid] = excl;
+    offsets[tid] = excl;
+  }
+  if (tid == E - 1) offsets[E] = excl + v;
+  __syncthreads();
+  if (active) {
+    int run = tot[e] + part[s * E + e];
+    for (int c = c0; c < c1; ++c) {
+      chunk_base[(size_t)c * E + e] = run;
+      run += chunk_counts[(size_t)c * E + e];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __restrict__ idx, long long N, int k, int E,
+                                                             int n_chunks, const int32_t* __restrict__ chunk_base,
+                                                             int32_t* __restrict__ perm_tok,
+                                                             int32_t* __restrict__ inv_pos) {
+  extern __shared__ int sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * WARPS + warp;
+  if (chunk >= n_chunks) return;
+  int* run = sh + warp * E;
+  for (int e = lane; e < E; e += 32) run[e] = __ldg(chunk_base + (size_t)chunk * E + e);
+  __syncwarp();
+  const long long base = (long long)chunk * CHUNK;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < CHUNK / 32; ++r) {
+    const long long i = base + r * 32 + lane;
+    int e = -1;
+    if (i < N) {
+      e = __ldg(idx + i);
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned m = __match_any_sync(FULL, e);
+    if (i < N) {
+      if (e >= 0) {
+        const int pos = run[e] + __popc(m & lt);
+        perm_tok[pos] = (int32_t)(i / k);
+        inv_pos[i] = pos;
+      } else {
+        inv_pos[i] = -1;
+      }
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) run[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, const int32_t* __restrict__ perm_tok,
+                                                     long long rows, int vec_per_row, long long T,
+                                                     V* __restrict__ xp) {
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long p = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; p < rows; p += warps) {
+    const int t = __ldg(perm_tok + p);
+    V* dst = xp + (size_t)p * vec_per_row;
+    if (t < 0 || t >= T) continue;   // only after an expert-id error; that is flagged already
+    const V* src = x + (size_t)t * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+}  // namespace
+
+int dispatch_num_chunks(long long pairs) { return (int)((pairs + CHUNK - 1) / CHUNK); }
+
+cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32_t* chunk_counts, int32_t* chunk_base,
+                             int32_t* counts, int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint32_t* err,
+                             cudaStream_t st, int* launches) {
+  const long long N = (long long)T * k;
+  const int n_chunks = dispatch_num_chunks(N);
+  const unsigned blocks = (unsigned)((n_chunks + WARPS - 1) / WARPS);
+  const size_t shm = (size_t)WARPS * E * sizeof(int);
+  hist_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, E, n_chunks, chunk_counts, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int S = 1;
+  while (S * 2 * E <= 1024 && S * 2 <= n_chunks) S *= 2;
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, n_chunks, E, S, chunk_base, counts, offsets);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  permute_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, k, E, n_chunks, chunk_base, perm_tok, inv_pos);
+  g_launches += 3;
+  if (launches) *launches += 3;
+  return cudaGetLastError();
+}
+
+cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, int d, int elem_bytes,
+                        void* x_perm, cudaStream_t st) {
+  const long long row_bytes = (long long)d * elem_bytes;
+  const int threads = 256;
+  long long want = (rows * 32 + threads - 1) / threads;
+  const unsigned blocks = (unsigned)(want < 148LL * 16 ? want : 148LL * 16);
+  if (row_bytes % 16 == 0 && ((uintptr_t)x % 16 == 0) && ((uintptr_t)x_perm % 16 == 0)) {
+    gather_kernel<uint4><<<blocks, threads, 0, st>>>((const uint4*)x, perm_tok, rows, (int)(row_bytes / 16), T,
+                                                     (uint4*)x_perm);
+  } else if (row_bytes % 4 == 0) {
+    gather_kernel<uint32_t><<<blocks, threads, 0, st>>>((const uint32_t*)x, perm_tok, rows, (int)(row_bytes / 4), T,
+                                                        (uint32_t*)x_perm);
+  } else {
+    gather_kernel<uint16_t><<<blocks, threads, 0, st>>>((const uint16_t*)x, perm_tok, rows, (int)(row_bytes / 2), T,
+                                                        (uint16_t*)x_perm);
+  }
+  ++g_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,421 @@
+// Grouped bf16 GEMM on the sm_103a tensor cores (tcgen05.mma, accumulators in TMEM, operands
+// staged by TMA), for the expert matmuls of the MoE layer: one group per expert, each group a
+// contiguous block of rows of the permuted activations (page "Mixture of Experts: What
+// Actually Happens When a Token Hits the Router", Step 3: each expert processes its block as
+// one dense matmul; page "8.6 - Mixture of Experts (MoE)", section 2: the SwiGLU expert).
+//
+// Two epilogues:
+//   EPI_SWIGLU  h = (X W1) * SiLU(X W2), written as bf16.  One 128 x 256 MMA tile holds
+//               128 columns of X W1 next to the same 128 columns of X W2, so the pair is
+//               finished in registers without a round trip through memory.
+//   EPI_F32     out (+)= X W, written as float32 (expert W3, shared W3, router logits).
+//
+// Work decomposition: a persistent grid of one CTA per SM walks the tiles
+// (group, n-tile, m-tile) in that order (m fastest, so CTAs that run at the same time share
+// one weight tile and the weights are streamed from HBM about once).  Group sizes are read on
+// the device from `offsets`, so nothing is synchronised with the host.  Row tiles may run
+// past the end of their group: the extra rows belong to the next group (or lie beyond the
+// matrix and are zero-filled by TMA) and their results are not stored.
+//
+// Warp roles (256 threads): warp 0 lane 0 issues TMA loads into a 4-stage shared-memory
+// ring; warp 1 lane 0 issues tcgen05.mma into one of two 256-column TMEM accumulators;
+// warps 4-7 drain the other accumulator (tcgen05.ld) and store; warp 2 owns the TMEM
+// allocation; warp 3 builds the group table.  Every wait is bounded (kWaitLimitNs) and on a
+// timeout sets the device error word and unwinds.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;                   // rows per tile (MMA M)
+constexpr int BN = 256;                   // MMA N (EPI_F32: output columns; SWIGLU: 128 + 128)
+constexpr int BK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_TILE = BM * BK * 2;       // 16 KB, K-major, 128B-swizzled
+constexpr int B_SUB = BK * 64 * 2;        // 8 KB: 64 k-rows x 64 n-columns, MN-major, swizzled
+constexpr int B_TILE = 4 * B_SUB;         // 32 KB
+constexpr int STAGE = A_TILE + B_TILE;    // 48 KB
+constexpr int MAX_GROUPS = 1024;
+constexpr int TMEM_COLS = 512;            // two 256-column fp32 accumulators
+constexpr int THREADS = 256;
+constexpr uint32_t IDESC = idesc_bf16_f32_kmaj_a_mnmaj_b<BM, BN>();
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  int tile_start[MAX_GROUPS + 1];
+  int row_off[MAX_GROUPS + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + sizeof(Ctrl);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+struct Tile {
+  int g, row0, row_end, n_tile;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int G, int t) {
+  int lo = 0, hi = G;  // largest g with tile_start[g] <= t (always a non-empty group)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (c.tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile r;
+  r.g = lo;
+  const int rows = c.row_off[lo + 1] - c.row_off[lo];
+  const int mt = (rows + BM - 1) / BM;
+  const int local = t - c.tile_start[lo];
+  r.n_tile = local / mt;
+  r.row0 = c.row_off[lo] + (local - r.n_tile * mt) * BM;
+  r.row_end = c.row_off[lo + 1];
+  return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * STAGE);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.offsets ? a.G : 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.tfull[b], 1);
+      mbar_init(&c.tempty[b], 4);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB0);
+    prefetch_tensormap(&tmB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(&c.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    // Group table: row offsets (clamped to the output's rows) and the first tile of each group.
+    bool bad = false;
+    for (int base = 0; base <= G; base += 32) {
+      const int g = base + lane;
+      if (g <= G) {
+        int off = a.offsets ? __ldg(a.offsets + g) : (g == 0 ? 0 : a.M);
+        if (off < 0 || off > a.rows_cap) { bad = true; off = off < 0 ? 0 : a.rows_cap; }
+        c.row_off[g] = off;
+      }
+    }
+    __syncwarp();
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int tiles = 0;
+      if (g < G) {
+        const int rows = c.row_off[g + 1] - c.row_off[g];
+        if (rows < 0) bad = true;
+        tiles = rows > 0 ? ((rows + BM - 1) / BM) * a.n_tiles : 0;
+      }
+      int v = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (g < G) c.tile_start[g] = carry + v - tiles;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) c.tile_start[G] = carry;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, ERR_OFFSETS);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem = c.tmem_base;
+  const int total = c.tile_start[G];
+  const int num_kb = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(c, G, t);
+        const int z = a.offsets ? tl.g : a.b_z;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort)) {
+            flag_error(a.err, ERR_WAIT_PRODUCER);
+            c.abort = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + (size_t)s * STAGE;
+          uint8_t* sb = sa + A_TILE;
+          mbar_arrive_expect_tx(&c.full[s], STAGE);
+          armed |= 1u << s;
+          armed_parity = (armed_parity & ~(1u << s)) | (phase << s);
+          const int k0 = kb * BK;
+          tma_load_2d(sa, &tmA, &c.full[s], k0, tl.row0);
+          if (EPI == EPI_SWIGLU) {
+            const int n0 = tl.n_tile * (BN / 2);
+            tma_load_3d(sb + 0 * B_SUB, &tmB0, &c.full[s], n0, k0, z);
+            tma_load_3d(sb + 1 * B_SUB, &tmB0, &c.full[s], n0 + 64, k0, z);
+            tma_load_3d(sb + 2 * B_SUB, &tmB1, &c.full[s], n0, k0, z);
+            tma_load_3d(sb + 3 * B_SUB, &tmB1, &c.full[s], n0 + 64, k0, z);
+          } else {
+            const int n0 = tl.n_tile * BN;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * B_SUB, &tmB0, &c.full[s], n0 + 64 * j, k0, z);
+          }
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA's shared memory is released.
+        volatile int never = 0;
+        for (int i = 0; i < STAGES; ++i)
+          if (armed & (1u << i)) mbar_wait(&c.full[i], (armed_parity >> i) & 1u, &never);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      int s = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.full[s], phase, &c.abort)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
+          const uint32_t sb = sa + A_TILE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A: K-major rows of 128 B; a K step of 16 elements moves 32 B inside the swizzle atom.
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            // B: MN-major; 8-row k-groups 1024 B apart, 64-column n-blocks B_SUB apart;
+            // a K step of 16 rows moves 2048 B.
+            const uint64_t bd = sdesc_sw128(sb + kk * 2048, B_SUB, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+          }
+          umma_commit(&c.empty[s]);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&c.tfull[buf]);
+      }
+      if (!ok) {
+        flag_error(a.err, ERR_WAIT_MMA);
+        c.abort = 1;
+        // Wait for the MMAs already issued before TMEM is released.
+        umma_commit(&c.drain);
+        volatile int never = 0;
+        mbar_wait(&c.drain, 0, &never);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile tl = decode_tile(c, G, t);
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      // Warp-uniform decision: the TMEM loads below are .sync.aligned.
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort));
+      if (!got) {
+        if (lane == 0) flag_error(a.err, ERR_WAIT_EPILOGUE);
+        c.abort = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const int row = tl.row0 + q * 32 + lane;
+      const bool valid = row < tl.row_end;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (EPI == EPI_SWIGLU) {
+        uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t u[32], v[32];
+          tmem_ld_32cols(taddr + ch * 32, u);
+          tmem_ld_32cols(taddr + 128 + ch * 32, v);
+          tmem_ld_wait();
+          const int col0 = tl.n_tile * (BN / 2) + ch * 32;
+          if (valid) {
+            uint32_t hp[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              const float v0 = __uint_as_float(v[2 * i]), v1 = __uint_as_float(v[2 * i + 1]);
+              const float h0 = u0 * __fdividef(v0, 1.0f + __expf(-v0));
+              const float h1 = u1 * __fdividef(v1, 1.0f + __expf(-v1));
+              hp[i] = pack_bf16x2(h0, h1);
+            }
+            uint16_t* dst = out + (size_t)row * a.ldo + col0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (col0 + 8 * j + 8 <= a.N)
+                *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
+          }
+        }
+      } else {
+        float* out = reinterpret_cast<float*>(a.out);
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + ch * 32, r);
+          tmem_ld_wait();
+          const int col0 = tl.n_tile * BN + ch * 32;
+          if (valid) {
+            float* dst = out + (size_t)row * a.ldo + col0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (col0 + 4 * j + 4 <= a.N) {
+                float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                if (a.accumulate) {
+                  const float4 o = *reinterpret_cast<const float4*>(dst + 4 * j);
+                  v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                }
+                *reinterpret_cast<float4*>(dst + 4 * j) = v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty[buf]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A operand: rows x K bf16 row-major; box 64 (K) x 128 (rows), 128B swizzle.
+static bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// B operand: Z matrices of K x N bf16 row-major (N contiguous); box 64 (N) x 64 (K) x 1.
+static bool make_map_b(CUtensorMap* m, const void* ptr, long long Z, long long K, long long N) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)(Z > 0 ? Z : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
+  cuuint32_t box[3] = {64, BK, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <int EPI>
+static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const GemmArgs& a,
+                          cudaStream_t st) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  grouped_gemm_kernel<EPI><<<num_sms(), THREADS, SMEM_BYTES, st>>>(ma, mb0, mb1, a);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+// h[rows, N] (bf16) = (A W1) * SiLU(A W2), grouped.  A is [rows_cap, K] bf16; W1, W2 are
+// [Z][K][N] bf16.  N must be a multiple of 8, K a multiple of 8.
+cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, const void* W2, int Z, int N,
+                      const int* offsets, int G, int M_dense, int b_z, void* h, uint32_t* err, cudaStream_t st) {
+  CUtensorMap ma, mb0, mb1;
+  if (!tc::make_map_a(&ma, A, rows_cap, K) || !tc::make_map_b(&mb0, W1, Z, K, N) || !tc::make_map_b(&mb1, W2, Z, K, N))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
+  a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);
+  a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
+  return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+}
+
+// out[rows, N] (f32) (+)= A W, grouped.  A is [rows_cap, K] bf16; W is [Z][K][N] bf16.
+cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* W, int Z, int N, const int* offsets,
+                          int G, int M_dense, int b_z, float* out, long long ldo, int accumulate, uint32_t* err,
+                          cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!tc::make_map_a(&ma, A, rows_cap, K) || !tc::make_map_b(&mb, W, Z, K, N)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
+  a.n_tiles = (N + tc::BN - 1) / tc::BN;
+  a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
+  return tc::launch<EPI_F32>(ma, mb, mb, a, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,263 @@
+// Router of the MoE layer: logits l = x W_g (+ logit_bias), top-k on l (+ sel_bias), gates.
+//
+// Page "8.6 - Mixture of Experts (MoE)", section 2: router(x) = x W_g, the k experts with the
+// largest logits, gates normalised over the chosen k.  Page "Mixture-of-Experts Internals: A
+// Systems Engineer's Field Manual", section 2.1 (softmax, top-k, renormalise) and 3.3 (bias
+// for the choice only).  Page "Mixture-of-Experts, from the router to the all-to-all", "The
+// router" (sigmoid scores normalised among the selected).
+//
+// Softmax gates renormalised over the chosen set only need the chosen logits:
+// s_i / sum_{I} s_j = exp(l_i - m) / sum_{I} exp(l_j - m) for any m (the full-softmax
+// denominator cancels), so the kernels take m = the largest chosen logit.
+//
+// Selection is a warp-wide argmax repeated k times, ties going to the lower expert id.
+// Logits are float32, summed in a fixed order, so the result is run-to-run identical.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+extern thread_local int g_launches;
+
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Warp argmax of (value, index): larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(FULL, v, o);
+    const int oi = __shfl_xor_sync(FULL, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
+// Lane L holds logits of experts L, L+32, ..., in l[EPL] (unbiased) and key[EPL] (selection
+// keys).  Chooses k experts and writes idx/gate for token t.  Padding slots must carry
+// key = -inf and an index >= E (excluded through `valid`).
+template <int EPL>
+__device__ __forceinline__ void select_and_gate(const float (&l)[EPL], float (&key)[EPL], int E, int k, int scoring,
+                                                int t, int32_t* idx, float* gate) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (lane + 32 * i >= E) taken |= 1u << i;
+  int my_idx = 0;
+  float my_l = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (!(taken & (1u << i))) {
+        const int e = lane + 32 * i;
+        if (key[i] > bv || (key[i] == bv && e < bi)) { bv = key[i]; bi = e; }
+      }
+    }
+    warp_argmax(bv, bi);
+    const int owner = bi & 31, slot = bi >> 5;
+    float wl = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (i == slot) wl = l[i];
+    wl = __shfl_sync(FULL, wl, owner);
+    if (lane == owner) taken |= 1u << slot;
+    if (lane == j) { my_idx = bi; my_l = wl; }
+  }
+  float g;
+  if (scoring == 0) {
+    const float m = warp_max(lane < k ? my_l : -INFINITY);
+    const float ex = lane < k ? expf(my_l - m) : 0.f;
+    g = ex / warp_sum(ex);
+  } else {
+    const float s = lane < k ? 1.0f / (1.0f + expf(-my_l)) : 0.f;
+    g = s / warp_sum(s);
+  }
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_idx;
+    gate[(size_t)t * k + lane] = g;
+  }
+}
+
+// One warp per token: logits on CUDA cores (lane-strided over d, then a butterfly sum), then
+// top-k and gates.  E <= EM <= 32.
+template <typename T, int EM>
+__global__ void __launch_bounds__(256) route_fused_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
+                                                          const float* __restrict__ lb, const float* __restrict__ sb,
+                                                          int Tn, int d, int E, int k, int scoring, int32_t* idx,
+                                                          float* gate, uint32_t* err) {
+  const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= Tn) return;
+  const T* xr = x + (size_t)t * d;
+  float acc[EM];
+#pragma unroll
+  for (int e = 0; e < EM; ++e) acc[e] = 0.f;
+  for (int i = lane; i < d; i += 32) {
+    const float xv = load_as_float(xr + i);
+    const T* w = Wg + (size_t)i * E;
+#pragma unroll
+    for (int e = 0; e < EM; ++e)
+      if (e < E) acc[e] = fmaf(xv, load_as_float(w + e), acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < EM; ++e) acc[e] = warp_sum(acc[e]);
+  float l[1], key[1];
+  l[0] = 0.f;
+#pragma unroll
+  for (int e = 0; e < EM; ++e)
+    if (e == lane) l[0] = acc[e];
+  key[0] = -INFINITY;
+  if (lane < E) {
+    if (lb) l[0] += __ldg(lb + lane);
+    key[0] = sb ? l[0] + __ldg(sb + lane) : l[0];
+    if (!isfinite(l[0]) || isnan(key[0])) {
+      flag_error(err, ERR_ROUTE);
+      if (isnan(key[0])) key[0] = -INFINITY;
+    }
+  }
+  select_and_gate<1>(l, key, E, k, scoring, t, idx, gate);
+}
+
+// One warp per token over precomputed float32 logits [T][E].
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ lb,
+                                                         const float* __restrict__ sb, int Tn, int E, int k,
+                                                         int scoring, int32_t* idx, float* gate, uint32_t* err) {
+  const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= Tn) return;
+  const float* lr = logits + (size_t)t * E;
+  float l[EPL], key[EPL];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    l[i] = 0.f;
+    key[i] = -INFINITY;
+    if (e < E) {
+      l[i] = __ldg(lr + e);
+      if (lb) l[i] += __ldg(lb + e);
+      key[i] = sb ? l[i] + __ldg(sb + e) : l[i];
+      if (!isfinite(l[i]) || isnan(key[i])) {
+        bad = true;
+        if (isnan(key[i])) key[i] = -INFINITY;
+      }
+    }
+  }
+  if (bad) flag_error(err, ERR_ROUTE);
+  select_and_gate<EPL>(l, key, E, k, scoring, t, idx, gate);
+}
+
+// Logits on CUDA cores: 64 tokens x 64 experts per block, 4 x 4 per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) logits_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg, int Tn,
+                                                          int d, int E, float* __restrict__ logits) {
+  constexpr int BT = 64, BE = 64, BK = 16;
+  __shared__ float xs[BK][BT + 4];
+  __shared__ float ws[BK][BE + 4];
+  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += BK) {
+    for (int i = threadIdx.x; i < BT * BK; i += 256) {
+      const int r = i / BK, kk = i % BK;
+      const int tt = t0 + r, kx = k0 + kk;
+      xs[kk][r] = (tt < Tn && kx < d) ? load_as_float(x + (size_t)tt * d + kx) : 0.f;
+    }
+    for (int i = threadIdx.x; i < BK * BE; i += 256) {
+      const int kk = i / BE, c = i % BE;
+      const int kx = k0 + kk, e = e0 + c;
+      ws[kk][c] = (kx < d && e < E) ? load_as_float(Wg + (size_t)kx * E + e) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { av[i] = xs[kk][ty * 4 + i]; bv[i] = ws[kk][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int tt = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
+      if (tt < Tn && e < E) logits[(size_t)tt * E + e] = acc[i][j];
+    }
+}
+
+}  // namespace
+
+cudaError_t route_fused(int dtype, const void* x, const void* W_g, const float* logit_bias, const float* sel_bias,
+                        int T, int d, int E, int k, int scoring, int32_t* idx, float* gate, uint32_t* err,
+                        cudaStream_t st) {
+  const int threads = 256;
+  const unsigned blocks = (unsigned)(((long long)T * 32 + threads - 1) / threads);
+#define MOE_ROUTE_FUSED(TY, EM)                                                                                    \
+  route_fused_kernel<TY, EM><<<blocks, threads, 0, st>>>((const TY*)x, (const TY*)W_g, logit_bias, sel_bias, T, d, \
+                                                         E, k, scoring, idx, gate, err)
+  if (dtype == 1) {
+    if (E <= 8) MOE_ROUTE_FUSED(uint16_t, 8);
+    else if (E <= 16) MOE_ROUTE_FUSED(uint16_t, 16);
+    else MOE_ROUTE_FUSED(uint16_t, 32);
+  } else {
+    if (E <= 8) MOE_ROUTE_FUSED(float, 8);
+    else if (E <= 16) MOE_ROUTE_FUSED(float, 16);
+    else MOE_ROUTE_FUSED(float, 32);
+  }
+#undef MOE_ROUTE_FUSED
+  ++g_launches;
+  return cudaGetLastError();
+}
+
+cudaError_t route_logits_simt(int dtype, const void* x, const void* W_g, int T, int d, int E, float* logits,
+                              cudaStream_t st) {
+  dim3 grid((E + 63) / 64, (T + 63) / 64);
+  if (dtype == 1)
+    logits_simt_kernel<uint16_t><<<grid, 256, 0, st>>>((const uint16_t*)x, (const uint16_t*)W_g, T, d, E, logits);
+  else
+    logits_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)x, (const float*)W_g, T, d, E, logits);
+  ++g_launches;
+  return cudaGetLastError();
+}
+
+cudaError_t route_topk(const float* logits, const float* logit_bias, const float* sel_bias, int T, int E, int k,
+                       int scoring, int32_t* idx, float* gate, uint32_t* err, cudaStream_t st) {
+  const int threads = 256;
+  const unsigned blocks = (unsigned)(((long long)T * 32 + threads - 1) / threads);
+#define MOE_TOPK(EPL) \
+  route_topk_kernel<EPL><<<blocks, threads, 0, st>>>(logits, logit_bias, sel_bias, T, E, k, scoring, idx, gate, err)
+  if (E <= 32) MOE_TOPK(1);
+  else if (E <= 64) MOE_TOPK(2);
+  else if (E <= 128) MOE_TOPK(4);
+  else if (E <= 256) MOE_TOPK(8);
+  else if (E <= 512) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
+  ++g_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

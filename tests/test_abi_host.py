@@ -1,0 +1,107 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every declared symbol, and rejects
+bad arguments with the documented status before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_sparse_02_b300 import build
+    build.build()
+    from mixture_experts_sparse_02_b300 import moe as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(moe):
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTS)
+
+
+def test_status_strings(moe):
+    for s in range(6):
+        assert moe.status_string(s) and moe.status_string(s) != "unknown status"
+
+
+def test_workspace_bytes(moe):
+    c = moe.config(4096, 4096, 14336, 8, 2)
+    big = moe.workspace_bytes(c)
+    assert big > 4096 * 2 * 4096 * 2  # at least x_perm
+    assert moe.workspace_bytes(moe.config(64, 4096, 14336, 8, 2)) < big
+    assert moe.workspace_bytes(moe.config(4, 64, 64, 8, 9)) == 0        # k > E: invalid
+    s = moe.workspace_bytes(moe.config(8192, 7168, 2048, 256, 8, scoring="sigmoid", n_shared=1, d_ff_shared=2048))
+    assert s > 8192 * 8 * 7168 * (2 + 4)
+
+
+FAKE = 0x100000  # a 16-byte aligned address that is never dereferenced: the checks return first
+
+
+def _fwd(moe, cfg, **over):
+    a = dict(x=FAKE, W_g=FAKE, W1=FAKE, W2=FAKE, W3=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40)
+    a.update(over)
+    ws_bytes = a.pop("ws_bytes")
+    try:
+        moe.forward(cfg, a.pop("x"), a.pop("W_g"), a.pop("W1"), a.pop("W2"), a.pop("W3"), a.pop("y"), a.pop("ws"),
+                    ws_bytes=ws_bytes, stream=0, **a)
+    except moe.MoEError as e:
+        return e.status
+    return moe.MOE_OK
+
+
+def test_argument_errors(moe):
+    ok = moe.config(16, 64, 64, 8, 2)
+    assert _fwd(moe, moe.config(16, 64, 64, 8, 9)) == moe.MOE_ERR_INVALID_ARG          # k > E
+    assert _fwd(moe, moe.config(16, 0, 64, 8, 2)) == moe.MOE_ERR_INVALID_ARG           # d = 0
+    assert _fwd(moe, moe.config(-1, 64, 64, 8, 2)) == moe.MOE_ERR_INVALID_ARG          # T < 0
+    assert _fwd(moe, moe.config(16, 64, 64, 2000, 2)) == moe.MOE_ERR_UNSUPPORTED       # E > 1024
+    assert _fwd(moe, moe.config(16, 64, 64, 64, 33)) == moe.MOE_ERR_UNSUPPORTED        # k > 32
+    assert _fwd(moe, moe.config(16, 60, 64, 8, 2)) == moe.MOE_ERR_UNSUPPORTED          # bf16 d % 8
+    assert _fwd(moe, ok, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert _fwd(moe, ok, x=FAKE + 2) == moe.MOE_ERR_INVALID_ARG                        # misaligned
+    assert _fwd(moe, ok, W3=None) == moe.MOE_ERR_INVALID_ARG
+    assert _fwd(moe, ok, ws=None) == moe.MOE_ERR_WORKSPACE
+    assert _fwd(moe, ok, ws_bytes=moe.workspace_bytes(ok) - 1) == moe.MOE_ERR_WORKSPACE
+    shared = moe.config(16, 64, 64, 8, 2, n_shared=1, d_ff_shared=64)
+    assert _fwd(moe, shared) == moe.MOE_ERR_INVALID_ARG                                # Ws* missing
+    bad_cfg = moe.config(16, 64, 64, 8, 2)
+    bad_cfg.dtype = 7
+    assert _fwd(moe, bad_cfg) == moe.MOE_ERR_INVALID_ARG
+    bad_cfg = moe.config(16, 64, 64, 8, 2)
+    bad_cfg.scoring = 5
+    assert _fwd(moe, bad_cfg) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_launches_nothing(moe):
+    assert _fwd(moe, moe.config(0, 64, 64, 8, 2), ws_bytes=0) == moe.MOE_OK
+    assert moe.last_launch_count() == 0
+
+
+def test_stage_argument_errors(moe):
+    cfg = moe.config(16, 64, 64, 64, 4)   # E > 32: moe_route needs a workspace for the logits
+    with pytest.raises(moe.MoEError) as e:
+        moe.route(cfg, FAKE, FAKE, FAKE, FAKE, ws=None, stream=0)
+    assert e.value.status == moe.MOE_ERR_WORKSPACE
+    with pytest.raises(moe.MoEError) as e:
+        moe.dispatch(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes=16, stream=0)
+    assert e.value.status == moe.MOE_ERR_WORKSPACE
+    with pytest.raises(moe.MoEError) as e:
+        moe.experts(cfg, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoEError) as e:
+        moe.combine(cfg, FAKE, FAKE, FAKE, None, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG

@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle, on seeded inputs.
+
+Routing indices, per-expert counts, offsets and the permutation must match bit for bit; the
+layer output within max|err| <= 2e-2 rms(ref) (bfloat16) or 1e-4 rms(ref) (float32).
+Small cases run the whole oracle; the five full-size workloads are checked on every
+routing decision and on sampled tokens' outputs, through the same moe_forward call that
+bench.py times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import Case
+from oracle import moe_oracle as orc
+
+from gpu_util import (GATE_ATOL, dev_to_f64, from_dev_stored, host_weight_fn, max_rel_err,
+                      require_cuda, tdtype, to_dev, upload_experts, y_tol)
+
+pytestmark = pytest.mark.gpu
+
+S = wl.MoEShape
+SMALL = [
+    wl.WORKLOADS["tiny_f32"],
+    S("bf16_softmax_ragged", T=300, d=512, d_ff=384, E=8, k=2, dtype="bf16", scoring="softmax"),
+    S("bf16_skewed_e64", T=257, d=256, d_ff=320, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.5),
+    S("bf16_sigmoid_shared_e256", T=200, d=384, d_ff=256, E=256, k=8, dtype="bf16", scoring="sigmoid",
+      n_shared=1, d_ff_shared=192),
+    S("bf16_k_equals_E", T=65, d=128, d_ff=136, E=4, k=4, dtype="bf16", scoring="softmax"),
+    S("bf16_E1_k1", T=130, d=64, d_ff=64, E=1, k=1, dtype="bf16", scoring="softmax"),
+    S("bf16_single_token", T=1, d=256, d_ff=256, E=16, k=4, dtype="bf16", scoring="softmax"),
+    S("bf16_two_shared_k1", T=96, d=192, d_ff=200, E=40, k=1, dtype="bf16", scoring="sigmoid",
+      n_shared=2, d_ff_shared=72),
+    S("f32_sigmoid_shared", T=50, d=96, d_ff=80, E=12, k=3, dtype="f32", scoring="sigmoid",
+      n_shared=2, d_ff_shared=48),
+    S("f32_e48", T=70, d=40, d_ff=24, E=48, k=5, dtype="f32", scoring="softmax", logit_bias_std=1.0),
+]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return require_cuda()
+
+
+def _device_inputs(case):
+    s = case.shape
+    d = {"x": to_dev(case.x, s), "W_g": to_dev(case.W_g, s)}
+    d["logit_bias"] = None if case.logit_bias is None else torch.from_numpy(case.logit_bias).cuda()
+    return d
+
+
+def _forward(moe, case, W, din):
+    s = case.shape
+    cfg = moe.config_from_shape(s)
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    moe.forward(cfg, din["x"], din["W_g"], W["W1"], W["W2"], W["W3"], y, ws, logit_bias=din["logit_bias"],
+                Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"), topk_idx_out=idx, counts_out=counts)
+    assert moe.get_device_error() == 0
+    return y, idx, counts
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_forward_small(moe, shape):
+    case = Case(shape, 0)
+    ref = case.forward()
+    W = upload_experts(shape, 0, keep=range(shape.E))
+    y, idx, counts = _forward(moe, case, W, _device_inputs(case))
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    err = max_rel_err(dev_to_f64(y), ref["y"])
+    assert err <= y_tol(shape), err
+    # run-to-run identical
+    y2, _, _ = _forward(moe, case, W, _device_inputs(case))
+    assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
+def test_stages_small(moe, shape):
+    """Each ABI call alone, fed the oracle's own intermediate results."""
+    s = shape
+    case = Case(s, 0)
+    ref = case.forward()
+    din = _device_inputs(case)
+    W = upload_experts(s, 0, keep=range(s.E))
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    # route
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    moe.route(cfg, din["x"], din["W_g"], idx, gate, logit_bias=din["logit_bias"], ws=ws)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.max(np.abs(gate.cpu().numpy() - ref["gate"])) <= GATE_ATOL
+    # dispatch (oracle indices in)
+    idx_ref = torch.from_numpy(ref["idx"]).cuda()
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.empty((s.T * s.k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((s.T * s.k, s.d), dtype=tdtype(s), device="cuda")
+    moe.dispatch(cfg, idx_ref, din["x"], counts, offsets, perm, inv, x_perm, ws)
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(perm.cpu().numpy(), ref["perm_tok"])
+    assert np.array_equal(inv.cpu().numpy(), ref["inv_pos"])
+    assert np.array_equal(from_dev_stored(x_perm, s), case.x[ref["perm_tok"]])
+    # experts (oracle x_perm and offsets in)
+    xp_ref = to_dev(case.x[ref["perm_tok"]], s)
+    off_ref = torch.from_numpy(ref["offsets"]).cuda()
+    y_perm = torch.empty((s.T * s.k, s.d), dtype=torch.float32, device="cuda")
+    moe.experts(cfg, xp_ref, off_ref, W["W1"], W["W2"], W["W3"], y_perm, ws)
+    assert max_rel_err(dev_to_f64(y_perm), ref["y_perm"]) <= y_tol(s)
+    # combine (oracle y_perm, inv_pos, gates in)
+    yp_ref = torch.from_numpy(ref["y_perm"].astype(np.float32)).cuda()
+    inv_ref = torch.from_numpy(ref["inv_pos"]).cuda()
+    g_ref = torch.from_numpy(ref["gate"].astype(np.float32)).cuda()
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    moe.combine(cfg, yp_ref, inv_ref, g_ref, y, x=din["x"], Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"),
+                ws=ws)
+    assert max_rel_err(dev_to_f64(y), ref["y"]) <= y_tol(s)
+    assert moe.get_device_error() == 0
+
+
+FULL = ["mixtral_prefill", "mixtral_decode", "hunyuan_a13b", "deepseek_v3"]
+
+
+def _sample_tokens(idx, counts, T, n_random, seed=1):
+    r = np.random.default_rng(seed)
+    hot = int(np.argmax(counts))
+    nz = np.nonzero(counts)[0]
+    cold = int(nz[np.argmin(counts[nz])])
+    pick = [0, T - 1]
+    for e in (hot, cold):
+        pick += list(np.nonzero((idx == e).any(axis=1))[0][:2])
+    pick += list(r.choice(T, size=min(n_random, T), replace=False))
+    return np.unique(np.array(pick, dtype=np.int64))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size(moe, name):
+    s = wl.WORKLOADS[name]
+    case = Case(s, 0)
+    r = case.route()
+    dsp = orc.dispatch(r["idx"], s.E)
+    sample = _sample_tokens(r["idx"], dsp["counts"], s.T, 12 if s.E >= 256 else 24)
+    W = upload_experts(s, 0, keep=np.unique(r["idx"][sample]))
+    din = _device_inputs(case)
+    y, idx, counts = _forward(moe, case, W, din)
+    assert np.array_equal(idx.cpu().numpy(), r["idx"])
+    assert np.array_equal(counts.cpu().numpy(), dsp["counts"])
+    get_w = host_weight_fn(W["host"], s)
+    x64 = case.f64(case.x[sample])
+    y_ref = orc.forward_tokens(x64, r["idx"][sample], r["gate"][sample], get_w, s.n_shared)
+    err = max_rel_err(dev_to_f64(y[torch.from_numpy(sample).cuda()]), y_ref)
+    assert err <= y_tol(s), err
+    # routing and dispatch outputs of the separate calls, at full size
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    gate = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    moe.route(cfg, din["x"], din["W_g"], idx, gate, logit_bias=din["logit_bias"], ws=ws)
+    assert np.max(np.abs(gate.cpu().numpy() - r["gate"])) <= GATE_ATOL
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.empty((s.T * s.k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((s.T * s.k, s.d), dtype=tdtype(s), device="cuda")
+    moe.dispatch(cfg, idx, din["x"], counts, offsets, perm, inv, x_perm, ws)
+    assert np.array_equal(offsets.cpu().numpy(), dsp["offsets"])
+    assert np.array_equal(perm.cpu().numpy(), dsp["perm_tok"])
+    assert np.array_equal(inv.cpu().numpy(), dsp["inv_pos"])
+    rows = np.random.default_rng(2).choice(s.T * s.k, size=64, replace=False)
+    assert np.array_equal(from_dev_stored(x_perm[torch.from_numpy(rows).cuda()], s), case.x[dsp["perm_tok"][rows]])
+    assert moe.get_device_error() == 0
+
+
+def test_empty_batch(moe):
+    s = S("empty", T=0, d=128, d_ff=128, E=8, k=2, dtype="bf16", scoring="softmax")
+    cfg = moe.config_from_shape(s)
+    dummy = torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+    moe.forward(cfg, dummy, dummy, dummy, dummy, dummy, dummy, dummy)
+    assert moe.last_launch_count() == 0
+
+
+def test_bad_expert_id_sets_device_error(moe):
+    s = S("bad_ids", T=64, d=64, d_ff=64, E=8, k=2, dtype="bf16", scoring="softmax")
+    cfg = moe.config_from_shape(s)
+    x = torch.randn((s.T, s.d), device="cuda").to(torch.bfloat16)
+    idx = torch.arange(s.T * s.k, device="cuda", dtype=torch.int32).reshape(s.T, s.k) % s.E
+    idx[5, 1] = s.E + 3          # out of range: flagged by the kernel, the pair is skipped
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.zeros((s.T * s.k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((s.T * s.k, s.d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    moe.get_device_error()
+    moe.dispatch(cfg, idx, x, counts, offsets, perm, inv, x_perm, ws)
+    w = moe.get_device_error()
+    assert w & 1
+    assert int(counts.sum()) == s.T * s.k - 1
+    assert int(inv[5, 1]) == -1
+    assert moe.get_device_error() == 0   # cleared by the previous read
