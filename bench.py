@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE FFN forward pass (libmoe, C ABI) on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one moe_forward over one batch of T tokens of the workload (route, dispatch,
+grouped SwiGLU experts, combine), inputs resident in HBM, L2 flushed (256 MiB write) between
+steps, each step timed with CUDA events on the launching stream.  With N > 1 (torchrun, one
+rank per GPU) every rank runs its own batch with replicated weights (the layer is per-token,
+so tokens shard with no exchange): weak scaling, no collective on the data path.
+
+Rank 0 prints one JSON line.  `value` = tokens of all ranks / max-over-ranks device time.
+`e2e` is the same through moe_forward_host with x and y in pinned host memory.  `roofline`
+is the W1/W2 + SwiGLU grouped GEMM (the dominant kernel).  `cpu_baseline` is the CPU oracle
+on a bounded sample on this host.  `--impl reference` times that oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec on 1 B300; expert-GEMM % of bf16 peak; decode HBM GB/s"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+DECODE_WORKLOAD = "mixtral_decode"
+FLUSH_BYTES = 256 << 20
+
+# DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM on the default workload, from
+# one ncu capture (profiles/), valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+
+
+def _sha256(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.25)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
+                             "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample_step(shape, host, n_tokens: int, seed: int = 0) -> float:
+    """The CPU oracle, as it stands, on the first n_tokens tokens of the workload.  Returns the
+    wall seconds (input generation excluded)."""
+    from oracle import moe_oracle as orc
+    x64 = wl.to_f64(host["x"][:n_tokens], shape.dtype)
+    Wg = wl.to_f64(host["W_g"], shape.dtype)
+    get_w = orc.weights_from_arrays(host["weights"], shape.dtype)
+    t0 = time.perf_counter()
+    orc.forward(x64, Wg, get_w, shape.E, shape.k, shape.scoring, host.get("logit_bias"), None, shape.n_shared)
+    return time.perf_counter() - t0
+
+
+def host_inputs(shape, seed=0, x_seed=None):
+    w = {}
+    for name in ("W1", "W2", "W3") + (("Ws1", "Ws2", "Ws3") if shape.n_shared else ()):
+        w[name] = wl.gen_experts(shape, name, seed)
+    return {"x": wl.gen_x(shape, seed if x_seed is None else x_seed), "W_g": wl.gen_router(shape, seed),
+            "logit_bias": wl.gen_logit_bias(shape, seed), "weights": w}
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") in ("openblas", "mkl")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, shape, world, rank):
+    if rank != 0:
+        return 0
+    host = host_inputs(shape)
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample_step(shape, host, n_tok)
+    times = [oracle_sample_step(shape, host, n_tok) for _ in range(args.steps)]
+    total = sum(times)
+    value = n_tok * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator)",
+            "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "d_ff": shape.d_ff, "E": shape.E,
+                       "k": shape.k, "sampled_tokens_per_step": n_tok},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": "first %d tokens of the workload per step (fp32 router, fp64 experts)" % n_tok},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+def upload_weights(shape, torch, seed=0):
+    from concurrent.futures import ThreadPoolExecutor
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    W = {}
+    jobs = []
+    for name in ("W1", "W2", "W3") + (("Ws1", "Ws2", "Ws3") if shape.n_shared else ()):
+        n = shape.n_shared if name.startswith("Ws") else shape.E
+        rows, cols, _ = wl.expert_dims(shape, name)
+        W[name] = torch.empty((n, rows, cols), dtype=dt, device="cuda")
+        jobs += [(name, e) for e in range(n)]
+    host = {name: [None] * W[name].shape[0] for name in W}
+
+    def one(job):
+        name, e = job
+        a = wl.gen_expert(shape, name, e, seed)
+        host[name][e] = a
+        t = torch.from_numpy(a)
+        W[name][e].copy_(t.view(dt) if shape.dtype == "bf16" else t)
+
+    with ThreadPoolExecutor(16) as ex:
+        list(ex.map(one, jobs))
+    torch.cuda.synchronize()
+    return W, {k: np.stack(v) for k, v in host.items()}
+
+
+def to_dev(torch, a, shape):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if shape.dtype == "bf16":
+        t = t.view(torch.bfloat16)
+    return t.cuda()
+
+
+def traffic_for_kernel():
+    src = os.path.join(ROOT, "mixture_experts_sparse_02_b300", "csrc", "gemm_tc.cu")
+    if NCU_TRAFFIC["source_sha256"] and os.path.exists(src) and _sha256(src) == NCU_TRAFFIC["source_sha256"]:
+        return NCU_TRAFFIC["bytes_per_launch"]
+    return None
+
+
+def run_ours(args, shape, world, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mixture_experts_sparse_02_b300 import moe
+
+    pk = peaks()
+    # replicated weights (seed 0); each rank draws its own tokens
+    W, W_host = upload_weights(shape, torch, 0)
+    x_host = wl.gen_x(shape, 0 if rank == 0 else 1000 + rank)
+    x = to_dev(torch, x_host, shape)
+    W_g = to_dev(torch, wl.gen_router(shape, 0), shape)
+    lb_np = wl.gen_logit_bias(shape, 0)
+    lb = None if lb_np is None else torch.from_numpy(lb_np).cuda()
+    cfg = moe.config_from_shape(shape)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    y = torch.empty((shape.T, shape.d), dtype=dt, device="cuda")
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    Ws = dict(Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"))
+
+    def step(events=None):
+        moe.forward(cfg, x, W_g, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb, events=events, **Ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if moe.get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_NUM_STAGES + 1)] for _ in range(args.steps)]
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+            launches += moe.last_launch_count()
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
+    stage_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(moe.MOE_NUM_STAGES)]
+                for i in range(args.steps)]
+    total_s = sum(step_ms) / 1e3
+    total_s_max = max_over_ranks(total_s, world, device="cuda")
+    tokens = shape.T * args.steps * world
+    value = tokens / total_s_max
+    mean_stage = [statistics.mean(s[j] for s in stage_ms) for j in range(moe.MOE_NUM_STAGES)]
+    stages = dict(zip(moe.STAGE_NAMES, [round(v, 4) for v in mean_stage]))
+
+    # algorithmic work
+    N = shape.T * shape.k
+    fl_w12 = 4.0 * N * shape.d * shape.d_ff
+    fl_w3 = 2.0 * N * shape.d * shape.d_ff
+    fl_sh = 6.0 * shape.T * shape.d * shape.d_ff_shared * shape.n_shared
+    t_w12 = mean_stage[2] / 1e3
+    t_w3 = mean_stage[3] / 1e3
+    t_sh = mean_stage[4] / 1e3
+    peak = pk["bf16_tflops"]
+    ach = fl_w12 / t_w12 / 1e12
+    roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<EPI_SWIGLU> (W1/W2 + SiLU*mul)",
+            "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(),
+            "algorithmic_flops_per_launch": fl_w12}
+    eg_t = t_w12 + t_w3 + t_sh
+    expert_tflops = (fl_w12 + fl_w3 + fl_sh) / eg_t / 1e12
+
+    # decode-shaped batch with the same weights (T = 16 tokens): touched-expert weight bytes / time
+    decode = None
+    if shape.name == DEFAULT_WORKLOAD and not args.no_decode:
+        dshape = wl.WORKLOADS[DECODE_WORKLOAD]
+        dcfg = moe.config_from_shape(dshape)
+        dws = torch.empty((moe.workspace_bytes(dcfg),), dtype=torch.uint8, device="cuda")
+        dx = x[: dshape.T].contiguous()
+        dy = torch.empty((dshape.T, dshape.d), dtype=dt, device="cuda")
+        counts = torch.empty((dshape.E,), dtype=torch.int32, device="cuda")
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            if i >= args.warmup:
+                dev_ev[i - args.warmup][0].record()
+            moe.forward(dcfg, dx, W_g, W["W1"], W["W2"], W["W3"], dy, dws, logit_bias=lb, counts_out=counts)
+            if i >= args.warmup:
+                dev_ev[i - args.warmup][1].record()
+        torch.cuda.synchronize()
+        dms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+        touched = int((counts.cpu() > 0).sum())
+        wbytes = touched * 3 * dshape.d * dshape.d_ff * 2 + dshape.d * dshape.E * 2
+        gbs = wbytes / (dms / 1e3) / 1e9
+        decode = {"workload": DECODE_WORKLOAD, "T": dshape.T, "ms_per_step": round(dms, 4),
+                  "touched_experts": touched, "touched_weight_bytes": wbytes, "hbm_gbs": round(gbs, 1),
+                  "peak_gbs": pk["hbm_gbs"], "frac": round(gbs / pk["hbm_gbs"], 4)}
+
+    # end to end through the public call with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(np.ascontiguousarray(x_host))
+        xh = (xh.view(torch.bfloat16) if shape.dtype == "bf16" else xh).pin_memory()
+        yh = torch.empty((shape.T, shape.d), dtype=dt).pin_memory()
+        for _ in range(max(1, args.warmup)):
+            moe.forward_host(cfg, xh, W_g, W["W1"], W["W2"], W["W3"], yh, ws, logit_bias=lb, **Ws)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            moe.forward_host(cfg, xh, W_g, W["W1"], W["W2"], W["W3"], yh, ws, logit_bias=lb, **Ws)
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, device="cuda")
+        nbytes = shape.T * shape.d * (2 if shape.dtype == "bf16" else 4)
+        e2e = {"value": shape.T * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+               "d2h_bytes_per_step": nbytes, "call": "moe_forward_host"}
+
+    # CPU oracle baseline on a bounded sample (rank 0 at N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {"x": x_host, "W_g": wl.gen_router(shape, 0), "logit_bias": lb_np, "weights": W_host}
+        n_tok = args.ref_tokens
+        t = oracle_sample_step(shape, host, n_tok)
+        cpu = {"value": n_tok / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": "first %d of %d tokens, one pass (fp32 router, fp64 experts), %.1f s" % (n_tok, shape.T, t)}
+
+    err = moe.get_device_error()
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s_max / args.steps, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
+                "data": "synthetic (seeded: x ~ N(0,1), weights ~ N(0,1/fan_in); per-rank tokens, replicated weights)",
+                "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "d_ff": shape.d_ff, "E": shape.E,
+                           "k": shape.k, "scoring": shape.scoring, "n_shared": shape.n_shared,
+                           "tokens_per_gpu": shape.T, "parallelism": "replicas (token shards)" if world > 1 else "1 GPU",
+                           "l2": "flushed between steps (256 MiB write)"},
+                "roofline": roof,
+                "expert_gemm": {"tflops": round(expert_tflops, 2), "frac_of_peak": round(expert_tflops / peak, 4),
+                                "peak_tflops": peak},
+                "decode": decode, "stages_ms": stages, "e2e": e2e, "cpu_baseline": cpu,
+                "gpu_launches": launches, "clocks": clk.summary(), "device_error_word": err}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--ref-tokens", type=int, default=64, help="tokens per CPU-oracle sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_env()
+    shape = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, shape, world, rank)
+    return run_ours(args, shape, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

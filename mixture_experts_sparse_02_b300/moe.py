@@ -148,7 +148,12 @@ def forward(cfg, x, W_g, W1, W2, W3, y, ws, logit_bias=None, sel_bias=None, Ws1=
     if events is None:
         _check(_forward(*args), "moe_forward")
     else:
-        arr = (ctypes.c_void_p * (MOE_NUM_STAGES + 1))(*[e.cuda_event if e is not None else None for e in events])
+        handles = []
+        for e in events:
+            if e is not None and not e.cuda_event:
+                e.record()          # torch creates its CUDA event lazily, on the first record
+            handles.append(e.cuda_event if e is not None else None)
+        arr = (ctypes.c_void_p * (MOE_NUM_STAGES + 1))(*handles)
         _check(_forward_profiled(*args, ctypes.cast(arr, ctypes.c_void_p)), "moe_forward_profiled")
 
 

@@ -169,7 +169,7 @@ def test_full_size(moe, name):
     assert np.array_equal(offsets.cpu().numpy(), dsp["offsets"])
     assert np.array_equal(perm.cpu().numpy(), dsp["perm_tok"])
     assert np.array_equal(inv.cpu().numpy(), dsp["inv_pos"])
-    rows = np.random.default_rng(2).choice(s.T * s.k, size=64, replace=False)
+    rows = np.random.default_rng(2).choice(s.T * s.k, size=min(64, s.T * s.k), replace=False)
     assert np.array_equal(from_dev_stored(x_perm[torch.from_numpy(rows).cuda()], s), case.x[dsp["perm_tok"][rows]])
     assert moe.get_device_error() == 0
 
