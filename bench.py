@@ -399,11 +399,15 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="", help="size overrides for profiling runs, e.g. T=2048,E=2,k=1")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_env()
     shape = wl.WORKLOADS[args.workload]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        shape = shape.replace(name=shape.name + "[" + args.override + "]", **{k: int(v) for k, v in kv.items()})
     if args.impl == "reference":
         return run_reference(args, shape, world, rank)
     return run_ours(args, shape, world, rank, local)
