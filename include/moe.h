@@ -200,6 +200,32 @@ int32_t moe_last_launch_count(void);
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
 
+/* Size of the library's own device scratch for moe_dispatch_static (bytes, per device). */
+#define MOE_DISPATCH_STATIC_SCRATCH_BYTES (1u << 20)
+
+/* moe_dispatch without a workspace: the same outputs as moe_dispatch, bit for bit, with its
+   scratch (the per-chunk count and position tables) taken from a fixed 1 MiB array that the
+   library keeps in device memory instead of from a caller-provided buffer.  The pages have
+   no counterpart for this call: it exists for callers that cannot allocate device memory
+   themselves, for example a plug-in whose host framework owns all device memory and hands
+   it no scratch, or a latency-critical path that must not call cudaMalloc (which can
+   synchronise the device).
+     Arguments and outputs are those of moe_dispatch minus ws/ws_bytes.
+     Size limit: ceil(T*k / 256) * E <= 131072 (the two tables fill at most 1 MiB), e.g.
+     T*k <= 131072 pairs with E = 256, or T*k <= 4194304 with E = 8.  Larger sizes return
+     MOE_ERR_UNSUPPORTED before anything is launched.
+     Allocation: none, on any call.  The array is part of the library's device image, so
+     every GPU that loads the library holds the 1 MiB until the process exits.  The first
+     call on each device looks up the array's device address (cudaGetSymbolAddress, with
+     that device current) and caches it; make that first call before any stream capture.
+     Sharing: every call on a device uses the same array, and a call overwrites what the
+     previous one left there before reading it.  Calls whose kernels overlap on the GPU
+     (different streams, no ordering between them) race on the array and give wrong
+     results: order them, or use moe_dispatch with separate workspaces. */
+moe_status moe_dispatch_static(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                               int32_t* counts, int32_t* offsets, int32_t* perm_tok,
+                               int32_t* inv_pos, void* x_perm, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

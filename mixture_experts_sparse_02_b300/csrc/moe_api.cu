@@ -8,6 +8,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "moe.h"
@@ -421,3 +423,52 @@ const char* moe_status_string(moe_status status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// moe_dispatch_static: moe_dispatch with its scratch in a fixed device array owned by the
+// library, for callers that cannot allocate device memory (see include/moe.h).
+
+namespace moe {
+
+constexpr size_t kStaticScratchInts = MOE_DISPATCH_STATIC_SCRATCH_BYTES / sizeof(int32_t);
+
+// The scratch itself: chunk counts followed by chunk positions.  Each dispatch call fully
+// rewrites the parts it reads (every chunk row of both tables), so nothing needs clearing.
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
+
+// Device address of g_dispatch_scratch, looked up once per device with that device current.
+// In host code the array's name is only a host-side stand-in and must not reach a kernel.
+static int32_t* dispatch_scratch_ptr() {
+  static std::mutex mu;
+  static int32_t* ptr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    int32_t* p = nullptr;
+    if (cudaGetSymbolAddress((void**)&p, g_dispatch_scratch) != cudaSuccess) return nullptr;
+    ptr[dev] = p;
+  }
+  return ptr[dev];
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_dispatch_static(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                                          int32_t* counts, int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos,
+                                          void* x_perm, moe_stream_t stream) {
+  g_launches = 0;
+  MOE_TRY(check_config(cfg));
+  const moe_config& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if (!topk_idx || !x || !counts || !offsets || !perm_tok || !inv_pos || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned4(topk_idx) || !aligned4(counts) || !aligned4(offsets) || !aligned4(perm_tok) || !aligned4(inv_pos) ||
+      !aligned16(x) || !aligned16(x_perm))
+    return MOE_ERR_INVALID_ARG;
+  const size_t table_ints = (size_t)dispatch_num_chunks((long long)c.T * c.k) * (size_t)c.E;
+  if (2 * table_ints > kStaticScratchInts) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = dispatch_scratch_ptr();
+  if (!scratch) return MOE_ERR_CUDA;
+  return stage_dispatch(c, topk_idx, x, counts, offsets, perm_tok, inv_pos, x_perm, scratch, scratch + table_ints,
+                        (cudaStream_t)stream);
+}

@@ -63,10 +63,12 @@ _forward_host = _sig("moe_forward_host", [_CFG] + [_P] * 12 + [_SZ, _P])
 _get_device_error = _sig("moe_get_device_error", [_P, ctypes.POINTER(ctypes.c_uint32)])
 _last_launch_count = _sig("moe_last_launch_count", [], ctypes.c_int32)
 _status_string = _sig("moe_status_string", [_I], ctypes.c_char_p)
+_dispatch_static = _sig("moe_dispatch_static", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P])
+DISPATCH_STATIC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts", "moe_combine",
            "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_get_device_error",
-           "moe_last_launch_count", "moe_status_string")
+           "moe_last_launch_count", "moe_status_string", "moe_dispatch_static")
 
 
 def status_string(status: int) -> str:
@@ -122,6 +124,13 @@ def dispatch(cfg, topk_idx, x, counts, offsets, perm_tok, inv_pos, x_perm, ws, w
     nb = ws.numel() * ws.element_size() if ws_bytes is None and ws is not None else (ws_bytes or 0)
     _check(_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
                      _ptr(inv_pos), _ptr(x_perm), _ptr(ws), nb, _stream(stream)), "moe_dispatch")
+
+
+def dispatch_static(cfg, topk_idx, x, counts, offsets, perm_tok, inv_pos, x_perm, stream=None):
+    """moe_dispatch without a workspace: for callers that cannot allocate device memory; the
+    scratch is a fixed 1 MiB array inside the library (size limit and sharing rules in moe.h)."""
+    _check(_dispatch_static(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
+                            _ptr(inv_pos), _ptr(x_perm), _stream(stream)), "moe_dispatch_static")
 
 
 def experts(cfg, x_perm, offsets, W1, W2, W3, y_perm, ws, ws_bytes=None, stream=None):
