@@ -40,7 +40,8 @@ FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM on the default workload, from
 # one ncu capture (profiles/), valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+NCU_TRAFFIC = {"source_sha256": "586062c6d25a549d7593ea7e673c47abf12cc2bff9a02476b4c1642616cf4fe1",
+               "bytes_per_launch": 2169.6e6}
 
 
 def _sha256(path):

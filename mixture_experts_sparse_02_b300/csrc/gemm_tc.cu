@@ -386,6 +386,7 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const C
     configured_device = dev;
   }
   grouped_gemm_kernel<EPI><<<num_sms(), THREADS, SMEM_BYTES, st>>>(ma, mb0, mb1, a);
+  ++g_launches;
   return cudaGetLastError();
 }
 

@@ -58,8 +58,15 @@ def _forward(moe, case, W, din):
     ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
     moe.forward(cfg, din["x"], din["W_g"], W["W1"], W["W2"], W["W3"], y, ws, logit_bias=din["logit_bias"],
                 Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"), topk_idx_out=idx, counts_out=counts)
+    assert moe.last_launch_count() == _expected_launches(s)
     assert moe.get_device_error() == 0
     return y, idx, counts
+
+
+def _expected_launches(s):
+    """Kernels one moe_forward launches: router (logits + top-k when E > 32), dispatch (histogram,
+    scan, permute, gather), W1/W2, W3, two per shared expert, combine."""
+    return (1 if s.E <= 32 else 2) + 4 + 2 + 2 * s.n_shared + 1
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
