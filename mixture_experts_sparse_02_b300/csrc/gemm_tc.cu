@@ -23,6 +23,8 @@
 // allocation; warp 3 builds the group table.  Every wait is bounded (kWaitLimitNs) and on a
 // timeout sets the device error word and unwinds.
 #include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -62,7 +64,8 @@ struct Tile {
   int g, row0, row_end, n_tile;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int G, int t) {
+template <int TILE_M = BM, typename C>
+__device__ __forceinline__ Tile decode_tile(const C& c, int G, int t) {
   int lo = 0, hi = G;  // largest g with tile_start[g] <= t (always a non-empty group)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -71,12 +74,108 @@ __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int G, int t) {
   Tile r;
   r.g = lo;
   const int rows = c.row_off[lo + 1] - c.row_off[lo];
-  const int mt = (rows + BM - 1) / BM;
+  const int mt = (rows + TILE_M - 1) / TILE_M;
   const int local = t - c.tile_start[lo];
   r.n_tile = local / mt;
-  r.row0 = c.row_off[lo] + (local - r.n_tile * mt) * BM;
+  r.row0 = c.row_off[lo] + (local - r.n_tile * mt) * TILE_M;
   r.row_end = c.row_off[lo + 1];
   return r;
+}
+
+// Warp-wide: the group table of a persistent grouped GEMM.  row_off[g] = offsets[g] clamped
+// to the output's rows (a violation is flagged), tile_start[g] = first tile of group g, with
+// ceil(rows / TILE_M) row tiles times n_tiles column tiles per non-empty group.
+template <int TILE_M, typename C>
+__device__ __forceinline__ void build_group_table(C& c, const GemmArgs& a, int G, int lane) {
+  bool bad = false;
+  for (int base = 0; base <= G; base += 32) {
+    const int g = base + lane;
+    if (g <= G) {
+      int off = a.offsets ? __ldg(a.offsets + g) : (g == 0 ? 0 : a.M);
+      if (off < 0 || off > a.rows_cap) { bad = true; off = off < 0 ? 0 : a.rows_cap; }
+      c.row_off[g] = off;
+    }
+  }
+  __syncwarp();
+  int carry = 0;
+  for (int base = 0; base < G; base += 32) {
+    const int g = base + lane;
+    int tiles = 0;
+    if (g < G) {
+      const int rows = c.row_off[g + 1] - c.row_off[g];
+      if (rows < 0) bad = true;
+      tiles = rows > 0 ? ((rows + TILE_M - 1) / TILE_M) * a.n_tiles : 0;
+    }
+    int v = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (g < G) c.tile_start[g] = carry + v - tiles;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) c.tile_start[G] = carry;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, ERR_OFFSETS);
+}
+
+// Epilogue of one accumulator tile for the 32 rows of this warp's TMEM lane quarter: read the
+// 256 fp32 columns at `taddr` (tcgen05.ld, warp-collective) and store row `row` when `valid`.
+//   EPI_SWIGLU: columns 0-127 hold X W1, 128-255 the same columns of X W2; h = u * SiLU(v) in bf16.
+//   EPI_F32:    256 output columns in float32, added to the existing values when accumulating.
+template <int EPI>
+__device__ __forceinline__ void drain_tile(const GemmArgs& a, uint32_t taddr, int row, bool valid, int n_tile) {
+  if (EPI == EPI_SWIGLU) {
+    uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t u[32], v[32];
+      tmem_ld_32cols(taddr + ch * 32, u);
+      tmem_ld_32cols(taddr + 128 + ch * 32, v);
+      tmem_ld_wait();
+      const int col0 = n_tile * (BN / 2) + ch * 32;
+      if (valid) {
+        uint32_t hp[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+          const float v0 = __uint_as_float(v[2 * i]), v1 = __uint_as_float(v[2 * i + 1]);
+          const float h0 = u0 * __fdividef(v0, 1.0f + __expf(-v0));
+          const float h1 = u1 * __fdividef(v1, 1.0f + __expf(-v1));
+          hp[i] = pack_bf16x2(h0, h1);
+        }
+        uint16_t* dst = out + (size_t)row * a.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (col0 + 8 * j + 8 <= a.N)
+            *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
+      }
+    }
+  } else {
+    float* out = reinterpret_cast<float*>(a.out);
+#pragma unroll 1
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t r[32];
+      tmem_ld_32cols(taddr + ch * 32, r);
+      tmem_ld_wait();
+      const int col0 = n_tile * BN + ch * 32;
+      if (valid) {
+        float* dst = out + (size_t)row * a.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (col0 + 4 * j + 4 <= a.N) {
+            float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            if (a.accumulate) {
+              const float4 o = *reinterpret_cast<const float4*>(dst + 4 * j);
+              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *reinterpret_cast<float4*>(dst + 4 * j) = v;
+          }
+        }
+      }
+    }
+  }
 }
 
 template <int EPI>
@@ -113,39 +212,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tmem_alloc(&c.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 3) {
-    // Group table: row offsets (clamped to the output's rows) and the first tile of each group.
-    bool bad = false;
-    for (int base = 0; base <= G; base += 32) {
-      const int g = base + lane;
-      if (g <= G) {
-        int off = a.offsets ? __ldg(a.offsets + g) : (g == 0 ? 0 : a.M);
-        if (off < 0 || off > a.rows_cap) { bad = true; off = off < 0 ? 0 : a.rows_cap; }
-        c.row_off[g] = off;
-      }
-    }
-    __syncwarp();
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int g = base + lane;
-      int tiles = 0;
-      if (g < G) {
-        const int rows = c.row_off[g + 1] - c.row_off[g];
-        if (rows < 0) bad = true;
-        tiles = rows > 0 ? ((rows + BM - 1) / BM) * a.n_tiles : 0;
-      }
-      int v = tiles;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-      }
-      if (g < G) c.tile_start[g] = carry + v - tiles;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) c.tile_start[G] = carry;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, ERR_OFFSETS);
-  }
+  if (warp == 3) build_group_table<BM>(c, a, G, lane);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -260,57 +327,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int row = tl.row0 + q * 32 + lane;
       const bool valid = row < tl.row_end;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (EPI == EPI_SWIGLU) {
-        uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t u[32], v[32];
-          tmem_ld_32cols(taddr + ch * 32, u);
-          tmem_ld_32cols(taddr + 128 + ch * 32, v);
-          tmem_ld_wait();
-          const int col0 = tl.n_tile * (BN / 2) + ch * 32;
-          if (valid) {
-            uint32_t hp[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-              const float v0 = __uint_as_float(v[2 * i]), v1 = __uint_as_float(v[2 * i + 1]);
-              const float h0 = u0 * __fdividef(v0, 1.0f + __expf(-v0));
-              const float h1 = u1 * __fdividef(v1, 1.0f + __expf(-v1));
-              hp[i] = pack_bf16x2(h0, h1);
-            }
-            uint16_t* dst = out + (size_t)row * a.ldo + col0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (col0 + 8 * j + 8 <= a.N)
-                *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
-          }
-        }
-      } else {
-        float* out = reinterpret_cast<float*>(a.out);
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t r[32];
-          tmem_ld_32cols(taddr + ch * 32, r);
-          tmem_ld_wait();
-          const int col0 = tl.n_tile * BN + ch * 32;
-          if (valid) {
-            float* dst = out + (size_t)row * a.ldo + col0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (col0 + 4 * j + 4 <= a.N) {
-                float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                if (a.accumulate) {
-                  const float4 o = *reinterpret_cast<const float4*>(dst + 4 * j);
-                  v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-                }
-                *reinterpret_cast<float4*>(dst + 4 * j) = v;
-              }
-            }
-          }
-        }
-      }
+      drain_tile<EPI>(a, taddr, row, valid, tl.n_tile);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.tempty[buf]);
@@ -322,6 +339,211 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------- CTA-pair kernel
+// The same grouped GEMM with one tcgen05.mma.cta_group::2 per 256 x 256 x 16 step shared by the
+// two CTAs of a cluster.  CTA r of the pair loads rows row0 + 128 r .. + 127 of A and MMA
+// columns 128 r .. 128 r + 127 of B (for SWIGLU: CTA 0 the W1 slice, CTA 1 the same slice of
+// W2; for EPI_F32: output columns n0 + 128 r ..) into its own shared memory, and receives its
+// 128 accumulator rows x 256 columns in its own tensor memory.  Per CTA a k-block stage is
+// 32 KB (A 16 KB + half of B 16 KB) instead of 48 KB, so six stages fit.
+//
+// Synchronisation: both CTAs' copies of a stage complete on full[s] in CTA 0, whose producer
+// expects 2 x 32 KB; the MMA thread (CTA 0 only) releases a stage to both producers with a
+// multicast commit on empty[s]; finished accumulators are signalled to both epilogues by a
+// multicast commit on tfull[b]; the eight epilogue warps of the pair release a buffer by
+// arriving on tempty[b] in CTA 0.
+namespace pair {
+constexpr int BM = 128;                   // rows per CTA
+constexpr int PAIR_M = 256;               // rows per pair tile (MMA M)
+constexpr int STAGES = 6;
+constexpr int A_TILE = BM * BK * 2;       // 16 KB
+constexpr int B_HALF = 2 * B_SUB;         // 16 KB: this CTA's 128 of the 256 MMA columns
+constexpr int STAGE = A_TILE + B_HALF;    // 32 KB
+constexpr uint32_t IDESC = idesc_bf16_f32_kmaj_a_mnmaj_b<PAIR_M, BN>();
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  int tile_start[MAX_GROUPS + 1];
+  int row_off[MAX_GROUPS + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + sizeof(Ctrl);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+}  // namespace pair
+
+// A bounded pause (used only after a timed-out wait, so that copies already issued can land
+// before the CTA's shared memory is released).
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
+  using pair::STAGES;
+  using pair::STAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  pair::Ctrl& c = *reinterpret_cast<pair::Ctrl*>(smem + (size_t)STAGES * STAGE);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.offsets ? a.G : 1;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = (int)(blockIdx.x >> 1);        // clusters are pairs of consecutive blocks
+  const int nclusters = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.tfull[b], 1);
+      mbar_init(&c.tempty[b], 8);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort = 0;
+    fence_barrier_init_cluster();
+    fence_proxy_async_smem();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB0);
+    prefetch_tensormap(&tmB1);
+  }
+  if (warp == 2) tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+  if (warp == 3) build_group_table<pair::PAIR_M>(c, a, G, lane);
+  tc_fence_before_sync();
+  cluster_sync();   // the peer's barriers are initialised and both CTAs hold their TMEM columns
+  tc_fence_after_sync();
+
+  const uint32_t tmem = c.tmem_base;
+  const int total = c.tile_start[G];
+  const int num_kb = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      int s = 0;
+      uint32_t phase = 0;
+      for (int t = cid; t < total; t += nclusters) {
+        const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
+        const int z = a.offsets ? tl.g : a.b_z;
+        const int arow = tl.row0 + (int)rank * pair::BM;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort)) {
+            flag_error(a.err, ERR_WAIT_PRODUCER);
+            c.abort = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + (size_t)s * STAGE;
+          uint8_t* sb = sa + pair::A_TILE;
+          if (rank == 0) mbar_arrive_expect_tx(&c.full[s], 2 * STAGE);
+          const uint32_t fb = mapa_shared(smem_addr(&c.full[s]), 0);
+          const int k0 = kb * BK;
+          tma_load_2d_pair(sa, &tmA, fb, k0, arow);
+          if (EPI == EPI_SWIGLU) {
+            const CUtensorMap* mb = rank == 0 ? &tmB0 : &tmB1;
+            const int n0 = tl.n_tile * (BN / 2);
+            tma_load_3d_pair(sb, mb, fb, n0, k0, z);
+            tma_load_3d_pair(sb + B_SUB, mb, fb, n0 + 64, k0, z);
+          } else {
+            const int n0 = tl.n_tile * BN + (int)rank * (BN / 2);
+            tma_load_3d_pair(sb, &tmB0, fb, n0, k0, z);
+            tma_load_3d_pair(sb + B_SUB, &tmB0, fb, n0 + 64, k0, z);
+          }
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (CTA 0)
+      int s = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += nclusters, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.full[s], phase, &c.abort)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
+          const uint32_t sb = sa + pair::A_TILE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // Same layouts as the single-CTA kernel; each CTA supplies its 128 rows of A and
+            // its two 64-column blocks of B at these shared-memory offsets.
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kk * 2048, B_SUB, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, pair::IDESC, (kb | kk) != 0);
+          }
+          umma_commit_pair(&c.empty[s], 0x3);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&c.tfull[buf], 0x3);
+      }
+      if (!ok) {
+        flag_error(a.err, ERR_WAIT_MMA);
+        c.abort = 1;
+        umma_commit_pair(&c.drain, 0x1);
+        volatile int never = 0;
+        mbar_wait(&c.drain, 0, &never);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t tempty0 = mapa_shared(smem_addr(&c.tempty[0]), 0);
+    const uint32_t tempty1 = mapa_shared(smem_addr(&c.tempty[1]), 0);
+    int it = 0;
+    for (int t = cid; t < total; t += nclusters, ++it) {
+      const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort));
+      if (!got) {
+        if (lane == 0) flag_error(a.err, ERR_WAIT_EPILOGUE);
+        c.abort = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const int row = tl.row0 + (int)rank * pair::BM + q * 32 + lane;
+      const bool valid = row < tl.row_end;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      drain_tile<EPI>(a, taddr, row, valid, tl.n_tile);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && c.abort) settle_after_abort();
+  tc_fence_before_sync();
+  cluster_sync();   // neither CTA leaves while the peer may still use its shared memory
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -390,6 +612,55 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const C
   return cudaGetLastError();
 }
 
+// Persistent grid of CTA pairs: as many clusters of 2 as can be resident at once (at most
+// half the SMs).
+template <int EPI>
+static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
+                               const GemmArgs& a, cudaStream_t st) {
+  static int configured_device = -1;
+  static int clusters = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pair::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    clusters = n < num_sms() / 2 ? n : num_sms() / 2;
+    configured_device = dev;
+  }
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, ma, mb0, mb1, a);
+  ++g_launches;
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Kernel choice: "pair" tiles are 256 rows, so they pay off when groups are large; the
+// single-CTA kernel (128-row tiles) wastes fewer rows on small or ragged groups.  The
+// environment variable MOE_GEMM_KERNEL=single|pair overrides the choice (used by the tests to
+// run both kernels on the same inputs).
+static bool use_pair(long long rows, int groups) {
+  const char* v = getenv("MOE_GEMM_KERNEL");
+  if (v && strcmp(v, "single") == 0) return false;
+  if (v && strcmp(v, "pair") == 0) return true;
+  return rows >= 512LL * (groups > 0 ? groups : 1);
+}
+
 }  // namespace tc
 
 // h[rows, N] (bf16) = (A W1) * SiLU(A W2), grouped.  A is [rows_cap, K] bf16; W1, W2 are
@@ -403,6 +674,8 @@ cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, 
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
   a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);
   a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
+  if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
+    return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
   return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
 }
 
@@ -416,6 +689,8 @@ cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* 
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
   a.n_tiles = (N + tc::BN - 1) / tc::BN;
   a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
+  if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
+    return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
   return tc::launch<EPI_F32>(ma, mb, mb, a, st);
 }
 

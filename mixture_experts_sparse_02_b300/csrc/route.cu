@@ -135,6 +135,157 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const T* __restrict__ 
   select_and_gate<1>(l, key, E, k, scoring, t, idx, gate);
 }
 
+// Sum NV per-lane partials over the 32 lanes of a warp by recursive halving: at each step a
+// lane keeps one half of its values, adds the peer's copy of that half and sends the other
+// half.  After min(5, log2 NV) steps lane L holds the complete sums of indices
+// base(L) .. base(L) + NV/2^steps - 1; if NV < 32 the remaining steps are plain butterflies, so
+// lanes that differ only in those low bits hold the same sums.  The order of additions is
+// fixed, so the result is run-to-run identical.
+template <int NV, int O>
+__device__ __forceinline__ void halve_sum(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (NV >= 2) {
+      constexpr int H = NV / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(FULL, send, O);
+      }
+      halve_sum<H, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(FULL, v[0], O);
+      halve_sum<1, O / 2>(v, lane);
+    }
+  }
+}
+
+// After halve_sum<NV, 16>: the first index a lane holds, and whether it is the lane that owns
+// those sums (its low bits, over which only plain butterflies ran, are zero).  NV is a power of 2.
+template <int NV>
+__device__ __forceinline__ int halve_base(int lane, bool& owner) {
+  constexpr int H = NV >= 32 ? 5 : NV >= 16 ? 4 : NV >= 8 ? 3 : NV >= 4 ? 2 : NV >= 2 ? 1 : 0;
+  int base = 0;
+#pragma unroll
+  for (int s = 0; s < H; ++s)
+    if (lane & (16 >> s)) base += NV >> (s + 1);
+  owner = (lane & ((1 << (5 - H)) - 1)) == 0;
+  return base;
+}
+
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int w) {
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// Element j of an array of 16-byte vectors holding bf16 (uint16_t) or float values.
+template <typename T> __device__ __forceinline__ float vec_elem(const uint4* a, int j);
+template <> __device__ __forceinline__ float vec_elem<uint16_t>(const uint4* a, int j) {
+  const uint32_t w = u4_word(a[j >> 3], (j >> 1) & 3);
+  return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+template <> __device__ __forceinline__ float vec_elem<float>(const uint4* a, int j) {
+  return __uint_as_float(u4_word(a[j >> 2], j & 3));
+}
+
+// Fused router for E in {1, 2, 4, 8, 16, 32}: a block of 8 warps takes TW tokens.  Every lane
+// reads 16-byte vectors of the TW token rows (VE elements of d each) and the VE matching rows
+// of W_g, strided over the block, so many loads are in flight and W_g is read once per TW
+// tokens.  The per-lane partial logits are summed over the warp (halve_sum) and then over the
+// 8 warps in warp order through shared memory.  Warp t then selects and gates token t.
+template <typename T, int E, int TW>
+__global__ void __launch_bounds__(256) route_vec_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
+                                                        const float* __restrict__ lb, const float* __restrict__ sb,
+                                                        int Tn, int d, int k, int scoring, int32_t* idx, float* gate,
+                                                        uint32_t* err) {
+  constexpr int VE = 16 / (int)sizeof(T);   // elements of d per 16-byte vector
+  constexpr int NV = TW * E;                // partial logits per lane, index t * E + e
+  constexpr int WG_VEC = E;                 // 16-byte vectors per VE rows of W_g (VE * E * sizeof(T) = 16 E)
+  __shared__ float red[8][NV];
+  __shared__ float logit[NV];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * TW;
+  float acc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+  const int nvec = d / VE;
+  const uint4* xv4 = reinterpret_cast<const uint4*>(x);
+  const uint4* wv4 = reinterpret_cast<const uint4*>(Wg);
+  const size_t row_vecs = (size_t)nvec;
+  constexpr int UNROLL = NV <= 32 ? 2 : 1;
+#pragma unroll UNROLL
+  for (int v = threadIdx.x; v < nvec; v += 256) {
+    uint4 xr[TW];
+#pragma unroll
+    for (int t = 0; t < TW; ++t)
+      xr[t] = (t0 + t < Tn) ? __ldg(xv4 + (size_t)(t0 + t) * row_vecs + v) : make_uint4(0, 0, 0, 0);
+    if constexpr ((E * sizeof(T)) % 16 == 0) {
+      // each of the VE rows of W_g is a whole number of 16-byte vectors: load row by row
+      constexpr int RV = E * (int)sizeof(T) / 16;
+#pragma unroll
+      for (int r = 0; r < VE; ++r) {
+        uint4 wr[RV];
+#pragma unroll
+        for (int i = 0; i < RV; ++i) wr[i] = __ldg(wv4 + ((size_t)v * VE + r) * RV + i);
+        float xe[TW];
+#pragma unroll
+        for (int t = 0; t < TW; ++t) xe[t] = vec_elem<T>(xr, t * VE + r);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float w = vec_elem<T>(wr, e);
+#pragma unroll
+          for (int t = 0; t < TW; ++t) acc[t * E + e] = fmaf(xe[t], w, acc[t * E + e]);
+        }
+      }
+    } else {
+      // small E: the VE rows together are E 16-byte vectors
+      uint4 wr[WG_VEC];
+#pragma unroll
+      for (int i = 0; i < WG_VEC; ++i) wr[i] = __ldg(wv4 + (size_t)v * WG_VEC + i);
+#pragma unroll
+      for (int r = 0; r < VE; ++r) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float w = vec_elem<T>(wr, r * E + e);
+#pragma unroll
+          for (int t = 0; t < TW; ++t) acc[t * E + e] = fmaf(vec_elem<T>(xr, t * VE + r), w, acc[t * E + e]);
+        }
+      }
+    }
+  }
+  halve_sum<NV, 16>(acc, lane);
+  constexpr int HN = NV >= 32 ? NV / 32 : 1;   // sums a lane holds after the halving
+  bool owner;
+  const int base = halve_base<NV>(lane, owner);
+  if (owner) {
+#pragma unroll
+    for (int i = 0; i < HN; ++i) red[warp][base + i] = acc[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < NV) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += red[w][threadIdx.x];
+    logit[threadIdx.x] = sum;
+  }
+  __syncthreads();
+  if (warp < TW && t0 + warp < Tn) {
+    float l[1], key[1];
+    l[0] = 0.f;
+    key[0] = -INFINITY;
+    if (lane < E) {
+      l[0] = logit[warp * E + lane];
+      if (lb) l[0] += __ldg(lb + lane);
+      key[0] = sb ? l[0] + __ldg(sb + lane) : l[0];
+      if (!isfinite(l[0]) || isnan(key[0])) {
+        flag_error(err, ERR_ROUTE);
+        if (isnan(key[0])) key[0] = -INFINITY;
+      }
+    }
+    select_and_gate<1>(l, key, E, k, scoring, t0 + warp, idx, gate);
+  }
+}
+
 // One warp per token over precomputed float32 logits [T][E].
 template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ lb,
@@ -214,6 +365,34 @@ cudaError_t route_fused(int dtype, const void* x, const void* W_g, const float* 
                         int T, int d, int E, int k, int scoring, int32_t* idx, float* gate, uint32_t* err,
                         cudaStream_t st) {
   const int threads = 256;
+  const int ve = dtype == 1 ? 8 : 4;
+  const bool vec = d % ve == 0 && ((uintptr_t)x % 16) == 0 && ((uintptr_t)W_g % 16) == 0 && (E & (E - 1)) == 0;
+  if (vec) {
+    // tokens per block: enough to reuse each W_g vector, few enough to keep the partials in registers
+    const int tw = E >= 32 ? 4 : E >= 8 ? 4 : 8;
+    const unsigned blocks = (unsigned)((T + tw - 1) / tw);
+#define MOE_ROUTE_VEC(TY, EE, TWW)                                                                                \
+  route_vec_kernel<TY, EE, TWW><<<blocks, threads, 0, st>>>((const TY*)x, (const TY*)W_g, logit_bias, sel_bias, T, \
+                                                            d, k, scoring, idx, gate, err)
+#define MOE_ROUTE_VEC_E(TY)                          \
+  switch (E) {                                       \
+    case 1: MOE_ROUTE_VEC(TY, 1, 8); break;          \
+    case 2: MOE_ROUTE_VEC(TY, 2, 8); break;          \
+    case 4: MOE_ROUTE_VEC(TY, 4, 8); break;          \
+    case 8: MOE_ROUTE_VEC(TY, 8, 4); break;          \
+    case 16: MOE_ROUTE_VEC(TY, 16, 4); break;        \
+    default: MOE_ROUTE_VEC(TY, 32, 4); break;        \
+  }
+    if (dtype == 1) {
+      MOE_ROUTE_VEC_E(uint16_t)
+    } else {
+      MOE_ROUTE_VEC_E(float)
+    }
+#undef MOE_ROUTE_VEC_E
+#undef MOE_ROUTE_VEC
+    ++g_launches;
+    return cudaGetLastError();
+  }
   const unsigned blocks = (unsigned)(((long long)T * 32 + threads - 1) / threads);
 #define MOE_ROUTE_FUSED(TY, EM)                                                                                    \
   route_fused_kernel<TY, EM><<<blocks, threads, 0, st>>>((const TY*)x, (const TY*)W_g, logit_bias, sel_bias, T, d, \
