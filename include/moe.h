@@ -105,13 +105,30 @@ size_t moe_workspace_bytes(const moe_config* cfg);
    section "The router" (sigmoid variant).
      x          [T][d] dtype            W_g [d][E] dtype
      logit_bias [E] float32 or NULL: added to the logits (enters scores and selection)
-     sel_bias   [E] float32 or NULL: added to the selection key only; gates stay unbiased
+     sel_bias   [E] float32 or NULL: a bias used for choosing only; gates stay unbiased.
+                The top-k is taken over logit + sel_bias for softmax routing, and over
+                sigmoid(logit) + sel_bias for sigmoid routing (the second page adds the bias
+                to DeepSeek-V3's sigmoid scores).  moe_update_sel_bias adjusts it.
      topk_idx   [T][k] int32 out: chosen experts in descending key order, ties -> lower id
      topk_gate  [T][k] float32 out
    ws: needs T*E*4 bytes (+ alignment) when E > 32, else may be NULL. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g,
                      const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
                      float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Auxiliary-loss-free balancing: one step of the selection-bias controller.
+   Page "Mixture-of-Experts Internals: A Systems Engineer's Field Manual", section 3.3, and
+   page "Mixture-of-Experts, from the router to the all-to-all", "Load balancing": after each
+   batch, an expert that received more than its share of the assignments has its bias
+   lowered by gamma, one that received less has it raised by gamma; an expert at exactly its
+   share keeps its bias.  The share is T*k/E, compared in integers (counts[e]*E against T*k).
+     counts   [E] int32 in: the last batch's per-expert assignment counts (moe_dispatch's
+              counts, or moe_forward's counts_out), for a batch of cfg->T tokens
+     gamma    step size (finite, >= 0)
+     sel_bias [E] float32 in/out: updated in place, in float32
+   One tiny kernel on `stream`; no workspace. */
+moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* counts, float gamma, float* sel_bias,
+                               moe_stream_t stream);
 
 /* Dispatch: per-expert histogram, exclusive prefix sum, stable permutation, row gather.
    Page "Mixture of Experts: What Actually Happens When a Token Hits the Router", Step 3

@@ -54,6 +54,10 @@ cudaError_t route_logits_simt(int dtype, const void* x, const void* W_g, int T, 
 cudaError_t route_topk(const float* logits, const float* logit_bias, const float* sel_bias, int T, int E, int k,
                        int scoring, int32_t* idx, float* gate, uint32_t* err, cudaStream_t st);
 
+// One step of the selection-bias controller from the last batch's per-expert counts.
+cudaError_t update_sel_bias(const int32_t* counts, int T, int k, int E, float gamma, float* sel_bias,
+                            cudaStream_t st);
+
 // ---- dispatch
 int dispatch_num_chunks(long long pairs);
 cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32_t* chunk_counts,

@@ -5,6 +5,7 @@
 // "Mixture-of-Experts, from the router to the all-to-all" (section "Expert parallelism and
 // the all-to-all"); on one GPU both exchanges are local: dispatch is a permutation of rows
 // and combine a gate-weighted gather back to token order.
+#include <math.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -286,6 +287,15 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g, cons
   }
   return stage_route(c, x, W_g, logit_bias, sel_bias, topk_idx, topk_gate, static_cast<float*>(ws),
                      (cudaStream_t)stream);
+}
+
+moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* counts, float gamma, float* sel_bias,
+                               moe_stream_t stream) {
+  g_launches = 0;
+  MOE_TRY(check_config(cfg));
+  if (!counts || !sel_bias || !aligned4(counts) || !aligned4(sel_bias)) return MOE_ERR_INVALID_ARG;
+  if (!(gamma >= 0.0f) || !isfinite(gamma)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(update_sel_bias(counts, cfg->T, cfg->k, cfg->E, gamma, sel_bias, (cudaStream_t)stream));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x, int32_t* counts,

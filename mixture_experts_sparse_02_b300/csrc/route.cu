@@ -47,6 +47,17 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// The value the top-k is taken over.  Without a selection bias: the logit (softmax and
+// sigmoid are monotone).  With a bias b used for choosing only: logit + b for softmax routing
+// (page "Mixture-of-Experts Internals: A Systems Engineer's Field Manual", section 3.3) and
+// sigmoid(logit) + b for sigmoid routing (page "Mixture-of-Experts, from the router to the
+// all-to-all", "Load balancing"), in float32.
+__device__ __forceinline__ float selection_key(float l, const float* __restrict__ sb, int e, int scoring) {
+  if (!sb) return l;
+  const float b = __ldg(sb + e);
+  return scoring == 1 ? 1.0f / (1.0f + expf(-l)) + b : l + b;
+}
+
 // Lane L holds logits of experts L, L+32, ..., in l[EPL] (unbiased) and key[EPL] (selection
 // keys).  Chooses k experts and writes idx/gate for token t.  Padding slots must carry
 // key = -inf and an index >= E (excluded through `valid`).
@@ -126,7 +137,7 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const T* __restrict__ 
   key[0] = -INFINITY;
   if (lane < E) {
     if (lb) l[0] += __ldg(lb + lane);
-    key[0] = sb ? l[0] + __ldg(sb + lane) : l[0];
+    key[0] = selection_key(l[0], sb, lane, scoring);
     if (!isfinite(l[0]) || isnan(key[0])) {
       flag_error(err, ERR_ROUTE);
       if (isnan(key[0])) key[0] = -INFINITY;
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(256) route_vec_kernel(const T* __restrict__ x,
     if (lane < E) {
       l[0] = logit[warp * E + lane];
       if (lb) l[0] += __ldg(lb + lane);
-      key[0] = sb ? l[0] + __ldg(sb + lane) : l[0];
+      key[0] = selection_key(l[0], sb, lane, scoring);
       if (!isfinite(l[0]) || isnan(key[0])) {
         flag_error(err, ERR_ROUTE);
         if (isnan(key[0])) key[0] = -INFINITY;
@@ -305,7 +316,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     if (e < E) {
       l[i] = __ldg(lr + e);
       if (lb) l[i] += __ldg(lb + e);
-      key[i] = sb ? l[i] + __ldg(sb + e) : l[i];
+      key[i] = selection_key(l[i], sb, e, scoring);
       if (!isfinite(l[i]) || isnan(key[i])) {
         bad = true;
         if (isnan(key[i])) key[i] = -INFINITY;
@@ -359,7 +370,28 @@ __global__ void __launch_bounds__(256) logits_simt_kernel(const T* __restrict__ 
     }
 }
 
+// One step of the bias controller: an expert whose load is above its share T k / E has its
+// selection bias lowered by gamma, one below raised by gamma (page "Mixture-of-Experts
+// Internals: A Systems Engineer's Field Manual", section 3.3).  Loads are compared in integers.
+__global__ void __launch_bounds__(256) update_sel_bias_kernel(const int32_t* __restrict__ counts, int E,
+                                                              long long share, float gamma, float* sb) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const long long c = (long long)__ldg(counts + e) * E;
+  float b = sb[e];
+  if (c > share) b = __fsub_rn(b, gamma);
+  else if (c < share) b = __fadd_rn(b, gamma);
+  sb[e] = b;
+}
+
 }  // namespace
+
+cudaError_t update_sel_bias(const int32_t* counts, int T, int k, int E, float gamma, float* sel_bias,
+                            cudaStream_t st) {
+  update_sel_bias_kernel<<<(E + 255) / 256, 256, 0, st>>>(counts, E, (long long)T * k, gamma, sel_bias);
+  ++g_launches;
+  return cudaGetLastError();
+}
 
 cudaError_t route_fused(int dtype, const void* x, const void* W_g, const float* logit_bias, const float* sel_bias,
                         int T, int d, int E, int k, int scoring, int32_t* idx, float* gate, uint32_t* err,

@@ -64,11 +64,12 @@ _get_device_error = _sig("moe_get_device_error", [_P, ctypes.POINTER(ctypes.c_ui
 _last_launch_count = _sig("moe_last_launch_count", [], ctypes.c_int32)
 _status_string = _sig("moe_status_string", [_I], ctypes.c_char_p)
 _dispatch_static = _sig("moe_dispatch_static", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P])
+_update_sel_bias = _sig("moe_update_sel_bias", [_CFG, _P, ctypes.c_float, _P, _P])
 DISPATCH_STATIC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts", "moe_combine",
            "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_get_device_error",
-           "moe_last_launch_count", "moe_status_string", "moe_dispatch_static")
+           "moe_last_launch_count", "moe_status_string", "moe_dispatch_static", "moe_update_sel_bias")
 
 
 def status_string(status: int) -> str:
@@ -131,6 +132,13 @@ def dispatch_static(cfg, topk_idx, x, counts, offsets, perm_tok, inv_pos, x_perm
     scratch is a fixed 1 MiB array inside the library (size limit and sharing rules in moe.h)."""
     _check(_dispatch_static(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
                             _ptr(inv_pos), _ptr(x_perm), _stream(stream)), "moe_dispatch_static")
+
+
+def update_sel_bias(cfg, counts, gamma, sel_bias, stream=None):
+    """One step of the selection-bias controller: sel_bias[e] -= gamma where counts[e] is above
+    the share T*k/E, += gamma where below (in place, float32)."""
+    _check(_update_sel_bias(ctypes.byref(cfg), _ptr(counts), float(gamma), _ptr(sel_bias), _stream(stream)),
+           "moe_update_sel_bias")
 
 
 def experts(cfg, x_perm, offsets, W1, W2, W3, y_perm, ws, ws_bytes=None, stream=None):

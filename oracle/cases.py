@@ -33,7 +33,7 @@ def gapped_attempts(shape: wl.MoEShape, seed: int = 0, min_gap: float = 1e-3,
     for _ in range(max_rounds):
         xr = wl.to_f64(x[rows], shape.dtype)
         l = orc.router_logits(xr, Wg, lb)
-        key = l if sel_bias is None else (l + np.asarray(sel_bias, np.float32)).astype(np.float32)
+        key = orc.selection_keys(l, shape.scoring, sel_bias)
         bad = rows[orc.min_adjacent_gap(key, m) < min_gap]
         if bad.size == 0:
             return attempts

@@ -21,7 +21,8 @@ Sources (page title, section):
   [RA]  "Mixture-of-Experts, from the router to the all-to-all": "The router" (sigmoid
         scores normalised over the chosen k), "Experts, fine-grained and shared" (P_e =
         3 d d_ff, combination counts), "Why total and active parameters come apart",
-        "Capacity and token dropping".
+        "Capacity and token dropping", "Load balancing" (auxiliary loss, a bias used only
+        for choosing and its update).
   [TR]  "Mixture of Experts: What Actually Happens When a Token Hits the Router": Step 3
         (the masked per-expert loop; sort by expert, one matmul per expert, scatter back),
         Step 4 (down(silu(gate(x)) * up(x)), weighted sum).
@@ -96,19 +97,55 @@ def gates_from_scores(s64: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return sel / sel.sum(axis=-1, keepdims=True)
 
 
+def selection_keys(l32: np.ndarray, scoring: str, sel_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """The float32 values the top-k is taken over.
+
+    Without a selection bias: the logits l (softmax and sigmoid are monotone, so the chosen
+    set and its order are those of the scores).  With a per-expert bias b used for choosing
+    only: [FM] section 3.3 adds b to the routing logit (softmax routing); [RA] "Load
+    balancing" (a bias instead of a loss) adds b to the score s (DeepSeek-V3's sigmoid routing).  So the key is
+    l + b for softmax scoring and sigmoid(l) + b for sigmoid scoring, each sum rounded to
+    float32 (the sigmoid itself is rounded to float32 first)."""
+    l = np.asarray(l32, np.float32)
+    if sel_bias is None:
+        return l
+    b = np.asarray(sel_bias, np.float32)
+    if scoring == "sigmoid":
+        s32 = scores(l, "sigmoid").astype(np.float32)
+        return (s32 + b).astype(np.float32)
+    return (l + b).astype(np.float32)
+
+
 def route(x64: np.ndarray, Wg64: np.ndarray, k: int, scoring: str,
           logit_bias: Optional[np.ndarray] = None,
           sel_bias: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """Router logits -> scores -> top-k -> gates for every token.
 
-    Selection runs on l (+ sel_bias, a bias used for choosing only, [FM] section 3.3; the
-    gates come from the unbiased scores).  Returns idx [T, k] int32, gate [T, k] float64,
-    logits [T, E] float32."""
+    Selection runs on selection_keys (a bias used for choosing only, [FM] section 3.3, [RA]
+    "Load balancing"; the gates come from the unbiased scores).  Returns idx [T, k]
+    int32, gate [T, k] float64, logits [T, E] float32."""
     l = router_logits(x64, Wg64, logit_bias)
-    key = l if sel_bias is None else (l + np.asarray(sel_bias, np.float32)).astype(np.float32)
-    idx = select_topk(key, k)
+    idx = select_topk(selection_keys(l, scoring, sel_bias), k)
     g = gates_from_scores(scores(l, scoring), idx)
     return {"idx": idx, "gate": g, "logits": l}
+
+
+def update_sel_bias(sel_bias: np.ndarray, counts: np.ndarray, T: int, k: int, gamma: float) -> np.ndarray:
+    """One step of the bias controller ([FM] section 3.3; [RA] "Load balancing"):
+    an expert that received more than its share T k / E of the last batch's assignments
+    (overloaded) has its bias lowered by gamma, one that received less (underloaded) has it
+    raised by gamma; an expert at exactly its share keeps its bias.  The comparison is done
+    in integers (counts[e] E against T k); the update in float32."""
+    b = np.asarray(sel_bias, np.float32).copy()
+    c = np.asarray(counts, np.int64)
+    E = len(b)
+    share = np.int64(T) * np.int64(k)
+    g = np.float32(gamma)
+    over = c * E > share
+    under = c * E < share
+    b[over] = (b[over] - g).astype(np.float32)
+    b[under] = (b[under] + g).astype(np.float32)
+    return b
 
 
 # --------------------------------------------------------------------------------------

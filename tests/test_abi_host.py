@@ -105,3 +105,15 @@ def test_stage_argument_errors(moe):
     with pytest.raises(moe.MoEError) as e:
         moe.combine(cfg, FAKE, FAKE, FAKE, None, stream=0)
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_update_sel_bias_argument_errors(moe):
+    cfg = moe.config(16, 64, 64, 8, 2)
+    for counts, gamma, sb in ((None, 0.1, FAKE), (FAKE, 0.1, None), (FAKE + 2, 0.1, FAKE), (FAKE, -1.0, FAKE),
+                              (FAKE, float("nan"), FAKE), (FAKE, float("inf"), FAKE)):
+        with pytest.raises(moe.MoEError) as e:
+            moe.update_sel_bias(cfg, counts, gamma, sb, stream=0)
+        assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoEError) as e:
+        moe.update_sel_bias(moe.config(16, 64, 64, 8, 9), FAKE, 0.1, FAKE, stream=0)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG

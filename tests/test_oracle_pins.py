@@ -218,6 +218,59 @@ def check_selection_bias():
     assert np.allclose(out["gate"], sel / sel.sum(axis=1, keepdims=True), rtol=1e-12)
 
 
+def check_selection_bias_sigmoid_uses_scores():
+    # Sigmoid routing adds the bias to the score ([RA] "Load balancing"): logits (3, 0, -1),
+    # bias (0, 0.6, 0.3) -> keys sigmoid(l) + b = (0.9526, 1.1, 0.5689): top-2 = experts 1, 0.
+    # On logits + bias (3, 0.6, -0.7) the order would be 0, 1 instead.
+    l = np.array([[3.0, 0.0, -1.0]])
+    sb = np.array([0.0, 0.6, 0.3], np.float32)
+    out = orc.route(l, np.eye(3), 2, "sigmoid", sel_bias=sb)
+    assert out["idx"].tolist() == [[1, 0]]
+    s1, s0 = 0.5, 1.0 / (1.0 + math.exp(-3.0))
+    assert np.allclose(out["gate"], [[s1 / (s0 + s1), s0 / (s0 + s1)]], rtol=1e-12)
+    # softmax routing adds it to the logit: keys (3, 0.6, -0.7) -> experts 0, 1
+    out = orc.route(l, np.eye(3), 2, "softmax", sel_bias=sb)
+    assert out["idx"].tolist() == [[0, 1]]
+    # a zero bias changes nothing
+    r = _rng(22)
+    x = r.normal(size=(40, 5))
+    Wg = r.normal(size=(5, 7))
+    for sc in ("softmax", "sigmoid"):
+        a = orc.route(x, Wg, 3, sc)
+        b = orc.route(x, Wg, 3, sc, sel_bias=np.zeros(7, np.float32))
+        assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["gate"], b["gate"])
+
+
+def check_sel_bias_update_closed_form():
+    # T = 10 tokens, k = 2, E = 4: share T k / E = 5 per expert.  Overloaded -> - gamma,
+    # underloaded -> + gamma, exactly at the share -> unchanged ([FM] 3.3).
+    b = np.array([0.5, -0.25, 0.0, 1.0], np.float32)
+    out = orc.update_sel_bias(b, np.array([9, 5, 4, 2]), 10, 2, 0.125)
+    assert out.dtype == np.float32
+    assert out.tolist() == [0.375, -0.25, 0.125, 1.125]
+    # shares that are not integers: T k / E = 7 / 3
+    out = orc.update_sel_bias(np.zeros(3, np.float32), np.array([3, 2, 2]), 7, 1, 1.0)
+    assert out.tolist() == [-1.0, 1.0, 1.0]
+
+
+def check_bias_controller_balances():
+    # Loads skewed by a fixed per-expert logit offset; repeated route -> count -> update
+    # steps drive the most-loaded expert towards its share (the controller's purpose).
+    r = _rng(23)
+    T, E, k = 512, 8, 2
+    l = (r.normal(0, 1, (T, E)) + np.linspace(-2, 2, E)).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    def max_over_mean(bias):
+        idx = orc.route(l.astype(np.float64), np.eye(E), k, "softmax", sel_bias=bias)["idx"]
+        c = np.bincount(idx.ravel(), minlength=E)
+        return c, c.max() / (T * k / E)
+    c, start = max_over_mean(b)
+    for _ in range(300):
+        b = orc.update_sel_bias(b, c, T, k, 0.02)
+        c, m = max_over_mean(b)
+    assert start > 2.0 and m < 1.2, (start, m)
+
+
 def check_printed_values():
     G = json.load(open(GOLDEN))
     for c in G["combinations"]:
@@ -260,7 +313,8 @@ CHECKS = [check_router_logits_closed_form, check_scores_closed_forms, check_topk
           check_gate_invariants, check_gates_two_formulations, check_k_equals_E_is_dense_softmax,
           check_dispatch, check_swiglu_scalar_closed_form, check_swiglu_vs_loops,
           check_E1_k1_is_dense_swiglu, check_grouped_equals_bruteforce, check_shared_only,
-          check_selection_bias, check_printed_values]
+          check_selection_bias, check_selection_bias_sigmoid_uses_scores, check_sel_bias_update_closed_form,
+          check_bias_controller_balances, check_printed_values]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -309,6 +363,14 @@ def _topk_ascending(key32, k):                 # smallest instead of largest
     return np.argsort(np.asarray(key32, np.float32), axis=-1, kind="stable")[:, :k].astype(np.int32)
 
 
+def _bias_update_wrong_sign(sel_bias, counts, T, k, gamma):   # overloaded experts pushed up
+    return orc.__dict__["_orig_update_sel_bias"](sel_bias, counts, T, k, -gamma)
+
+
+def _bias_on_logits(l32, scoring, sel_bias=None):             # sigmoid bias added to logits
+    return orc.__dict__["_orig_selection_keys"](l32, "softmax", sel_bias)
+
+
 PLANTS = [
     ("swiglu_expert", _swapped_swiglu, [check_swiglu_scalar_closed_form, check_swiglu_vs_loops]),
     ("gates_from_scores", _no_renorm, [check_gate_invariants, check_gates_two_formulations]),
@@ -317,6 +379,8 @@ PLANTS = [
     ("shared_experts", _no_shared, [check_shared_only]),
     ("silu", _silu_sign, [check_swiglu_scalar_closed_form, check_E1_k1_is_dense_swiglu]),
     ("select_topk", _topk_ascending, [check_topk_bruteforce]),
+    ("update_sel_bias", _bias_update_wrong_sign, [check_sel_bias_update_closed_form, check_bias_controller_balances]),
+    ("selection_keys", _bias_on_logits, [check_selection_bias_sigmoid_uses_scores]),
 ]
 
 

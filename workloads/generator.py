@@ -154,6 +154,12 @@ def gen_logit_bias(shape: MoEShape, seed: int = 0) -> Optional[np.ndarray]:
     return standard_normal(seed, "logit_bias", 0, shape.E) * np.float32(shape.logit_bias_std)
 
 
+def gen_sel_bias(shape: MoEShape, std: float, seed: int = 0) -> np.ndarray:
+    """A per-expert selection bias [E] float32 ~ N(0, std^2) (a state of the balancing
+    controller, for tests that route with such a bias)."""
+    return standard_normal(seed, "sel_bias", 0, shape.E) * np.float32(std)
+
+
 def expert_dims(shape: MoEShape, which: str):
     """(rows, cols, std) of one expert matrix: W1/W2 are [d, d_ff], W3 is [d_ff, d]."""
     if which in ("W1", "W2"):
