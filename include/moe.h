@@ -74,7 +74,11 @@ typedef enum {
   MOE_SOFTMAX_TOPK_RENORM = 0,
   /* sigmoid per expert, top-k, normalise among the chosen k (page "Mixture-of-Experts,
      from the router to the all-to-all", section "The router", DeepSeek-V3) */
-  MOE_SIGMOID_TOPK_NORM = 1
+  MOE_SIGMOID_TOPK_NORM = 1,
+  /* softmax over all E, top-k, gates = the softmax probabilities themselves, not
+     renormalised; with k = 1 this is the Switch Transformer's y = p_i(x) E_i(x) (page
+     "Mixture-of-Experts, from the router to the all-to-all", section "The router") */
+  MOE_SOFTMAX_TOPK_PLAIN = 2
 } moe_scoring;
 
 typedef struct {
@@ -115,6 +119,24 @@ size_t moe_workspace_bytes(const moe_config* cfg);
 moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g,
                      const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
                      float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Forward load statistics of one batch.
+   Page "8.6 - Mixture of Experts (MoE)", section 3.1, and page "Mixture-of-Experts
+   Internals: A Systems Engineer's Field Manual", section 3.2 (the Switch balancing loss);
+   page "T2.6 What MoE changes", "Routing creates an assignment problem" and "In practice"
+   (per-expert counts and maximum-to-mean load are what to monitor).
+     x, W_g, logit_bias  the router's inputs, as for moe_route (the scores are recomputed)
+     counts     [E] int32 in: the batch's per-expert assignment counts (moe_dispatch output)
+     alpha      weight of the balancing loss
+     f          [E] float32 out: f_e = counts[e] / T, the fraction of tokens routed to e
+     P          [E] float32 out: P_e = mean over the T tokens of the score s_e (the softmax
+                over all E for the softmax scorings, the sigmoid for MOE_SIGMOID_TOPK_NORM)
+     summary    [2] float32 out: L_aux = alpha * E * sum_e f_e P_e, and max_e counts[e] / (T*k/E)
+   Needs T >= 1.  Sums are float32 in a fixed order (identical results from run to run).
+   ws: T*E*4 bytes for the logits plus a small per-block table (moe_workspace_bytes covers it). */
+moe_status moe_load_stats(const moe_config* cfg, const void* x, const void* W_g, const float* logit_bias,
+                          const int32_t* counts, float alpha, float* f, float* P, float* summary, void* ws,
+                          size_t ws_bytes, moe_stream_t stream);
 
 /* Auxiliary-loss-free balancing: one step of the selection-bias controller.
    Page "Mixture-of-Experts Internals: A Systems Engineer's Field Manual", section 3.3, and

@@ -58,6 +58,12 @@ cudaError_t route_topk(const float* logits, const float* logit_bias, const float
 cudaError_t update_sel_bias(const int32_t* counts, int T, int k, int E, float gamma, float* sel_bias,
                             cudaStream_t st);
 
+// ---- load statistics (f, P, L_aux, max/mean load) from float32 logits [T][E]
+int stats_num_blocks(int T);
+cudaError_t load_stats(const float* logits, const float* logit_bias, const int32_t* counts, int T, int k, int E,
+                       int scoring, float alpha, float* partial, float* f, float* P, float* summary,
+                       cudaStream_t st);
+
 // ---- dispatch
 int dispatch_num_chunks(long long pairs);
 cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32_t* chunk_counts,

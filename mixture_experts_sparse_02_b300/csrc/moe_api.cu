@@ -40,6 +40,7 @@ static int esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 // Bytes of each scratch region.
 struct Sizes {
   size_t logits, idx, gate, counts, offsets, chunk, perm, inv, x_perm, h, y_perm, hs, ys, x_io, y_io;
+  size_t stats_logits, stats_partial;   // moe_load_stats: logits [T][E] f32, per-block score sums
 };
 
 static Sizes sizes(const moe_config& c) {
@@ -60,6 +61,8 @@ static Sizes sizes(const moe_config& c) {
   s.ys = c.n_shared > 0 ? align_up(T * c.d * 4) : 0;
   s.x_io = align_up(T * c.d * esize(c));
   s.y_io = align_up(T * c.d * esize(c));
+  s.stats_logits = align_up(T * c.E * 4);
+  s.stats_partial = align_up((size_t)stats_num_blocks(c.T) * c.E * 4);
   return s;
 }
 
@@ -91,7 +94,8 @@ static FwdLayout fwd_layout(const moe_config& c) {
   L.y_io = o; o += s.y_io;
   L.shared_region = o;
   o += max4(s.logits, s.chunk, s.h, s.hs + s.ys);
-  L.total = o;
+  // moe_load_stats uses the workspace from its start
+  L.total = o > s.stats_logits + s.stats_partial ? o : s.stats_logits + s.stats_partial;
   return L;
 }
 
@@ -102,7 +106,9 @@ static moe_status check_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0 || c->k > c->E) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->scoring != MOE_SOFTMAX_TOPK_RENORM && c->scoring != MOE_SIGMOID_TOPK_NORM) return MOE_ERR_INVALID_ARG;
+  if (c->scoring != MOE_SOFTMAX_TOPK_RENORM && c->scoring != MOE_SIGMOID_TOPK_NORM &&
+      c->scoring != MOE_SOFTMAX_TOPK_PLAIN)
+    return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || (c->n_shared > 0 && c->d_ff_shared <= 0)) return MOE_ERR_INVALID_ARG;
   if (c->E > 1024 || c->k > 32) return MOE_ERR_UNSUPPORTED;
   const long long N = (long long)c->T * c->k;
@@ -287,6 +293,34 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g, cons
   }
   return stage_route(c, x, W_g, logit_bias, sel_bias, topk_idx, topk_gate, static_cast<float*>(ws),
                      (cudaStream_t)stream);
+}
+
+moe_status moe_load_stats(const moe_config* cfg, const void* x, const void* W_g, const float* logit_bias,
+                          const int32_t* counts, float alpha, float* f, float* P, float* summary, void* ws,
+                          size_t ws_bytes, moe_stream_t stream) {
+  g_launches = 0;
+  MOE_TRY(check_config(cfg));
+  const moe_config& c = *cfg;
+  if (c.T == 0) return MOE_ERR_INVALID_ARG;   // the statistics are means over the batch
+  if (!x || !W_g || !counts || !f || !P || !summary) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned4(W_g) || !aligned4(counts) || !aligned4(f) || !aligned4(P) || !aligned4(summary))
+    return MOE_ERR_INVALID_ARG;
+  if (logit_bias && !aligned4(logit_bias)) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(alpha)) return MOE_ERR_INVALID_ARG;
+  const Sizes s = sizes(c);
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < s.stats_logits + s.stats_partial) return MOE_ERR_WORKSPACE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  float* logits = static_cast<float*>(ws);
+  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + s.stats_logits);
+  if (c.dtype == MOE_BF16 && c.E % 8 == 0 && aligned16(W_g)) {
+    MOE_CUDA(tc_matmul_f32(x, c.T, c.d, W_g, 1, c.E, nullptr, 1, c.T, 0, logits, c.E, 0, error_word(), st));
+  } else {
+    MOE_CUDA(route_logits_simt(c.dtype, x, W_g, c.T, c.d, c.E, logits, st));
+  }
+  return cuda_status(load_stats(logits, logit_bias, counts, c.T, c.k, c.E, c.scoring, alpha, partial, f, P, summary,
+                                st));
 }
 
 moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* counts, float gamma, float* sel_bias,

@@ -6,6 +6,7 @@
 // for the choice only).  Page "Mixture-of-Experts, from the router to the all-to-all", "The
 // router" (sigmoid scores normalised among the selected).
 //
+// Switch-style gates (softmax without renormalisation) need the full softmax denominator.
 // Softmax gates renormalised over the chosen set only need the chosen logits:
 // s_i / sum_{I} s_j = exp(l_i - m) / sum_{I} exp(l_j - m) for any m (the full-softmax
 // denominator cancels), so the kernels take m = the largest chosen logit.
@@ -96,6 +97,20 @@ __device__ __forceinline__ void select_and_gate(const float (&l)[EPL], float (&k
     const float m = warp_max(lane < k ? my_l : -INFINITY);
     const float ex = lane < k ? expf(my_l - m) : 0.f;
     g = ex / warp_sum(ex);
+  } else if (scoring == 2) {
+    // Switch-style: the softmax probability over all E itself, not renormalised (page
+    // "Mixture-of-Experts, from the router to the all-to-all", "The router": y = p_i(x) E_i(x))
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) m = fmaxf(m, l[i]);
+    m = warp_max(m);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) z += expf(l[i] - m);
+    z = warp_sum(z);
+    g = lane < k ? expf(my_l - m) / z : 0.f;
   } else {
     const float s = lane < k ? 1.0f / (1.0f + expf(-my_l)) : 0.f;
     g = s / warp_sum(s);

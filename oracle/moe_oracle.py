@@ -16,13 +16,17 @@ Sources (page title, section):
         (FLOP and parameter counts), section 3.1 (auxiliary loss), section 3.2 (capacity),
         section 4 (combinations), section 4.1 (shared expert).
   [FM]  "Mixture-of-Experts Internals: A Systems Engineer's Field Manual": section 2.1
-        (softmax over all E, top-k, renormalise over the chosen k), section 3.3 (bias used
-        only for selection), section 4.2 (dispatch volume).
+        (softmax over all E, top-k, renormalise over the chosen k), section 3.2 (Switch
+        auxiliary loss), section 3.3 (bias used only for selection), section 4.2 (dispatch
+        volume).
   [RA]  "Mixture-of-Experts, from the router to the all-to-all": "The router" (sigmoid
-        scores normalised over the chosen k), "Experts, fine-grained and shared" (P_e =
+        scores normalised over the chosen k; Switch's top-1 y = p_i(x) E_i(x) without
+        renormalisation), "Experts, fine-grained and shared" (P_e =
         3 d d_ff, combination counts), "Why total and active parameters come apart",
         "Capacity and token dropping", "Load balancing" (auxiliary loss, a bias used only
         for choosing and its update).
+  [T26] "T2.6 What MoE changes": "Routing creates an assignment problem" (per-expert counts,
+        maximum load over mean load), "In practice" (what to monitor).
   [TR]  "Mixture of Experts: What Actually Happens When a Token Hits the Router": Step 3
         (the masked per-expert loop; sort by expert, one matmul per expert, scatter back),
         Step 4 (down(silu(gate(x)) * up(x)), weighted sum).
@@ -68,10 +72,11 @@ def router_logits(x64: np.ndarray, Wg64: np.ndarray,
 def scores(l32: np.ndarray, scoring: str) -> np.ndarray:
     """Per-expert scores in float64.
 
-    softmax: s = softmax(l) over all E experts ([FM] section 2.1; [RA] "The router").
-    sigmoid: s_e = 1 / (1 + exp(-l_e)), DeepSeek-V3's scoring ([RA] "The router")."""
+    softmax (and softmax_norenorm): s = softmax(l) over all E experts ([FM] section 2.1;
+    [RA] "The router").  sigmoid: s_e = 1 / (1 + exp(-l_e)), DeepSeek-V3's scoring ([RA]
+    "The router")."""
     l = np.asarray(l32, np.float64)
-    if scoring == "softmax":
+    if scoring in ("softmax", "softmax_norenorm"):
         m = l.max(axis=-1, keepdims=True)
         e = np.exp(l - m)
         return e / e.sum(axis=-1, keepdims=True)
@@ -126,7 +131,12 @@ def route(x64: np.ndarray, Wg64: np.ndarray, k: int, scoring: str,
     int32, gate [T, k] float64, logits [T, E] float32."""
     l = router_logits(x64, Wg64, logit_bias)
     idx = select_topk(selection_keys(l, scoring, sel_bias), k)
-    g = gates_from_scores(scores(l, scoring), idx)
+    s = scores(l, scoring)
+    if scoring == "softmax_norenorm":
+        # Switch: y = p_i(x) E_i(x), the softmax probability itself ([RA] "The router")
+        g = np.take_along_axis(s, idx.astype(np.int64), axis=-1)
+    else:
+        g = gates_from_scores(s, idx)
     return {"idx": idx, "gate": g, "logits": l}
 
 
@@ -349,6 +359,24 @@ def aux_loss(f: np.ndarray, P: np.ndarray, alpha: float) -> float:
     f = np.asarray(f, np.float64)
     P = np.asarray(P, np.float64)
     return float(alpha * len(f) * np.sum(f * P))
+
+
+def load_stats(idx: np.ndarray, l32: np.ndarray, E: int, scoring: str, alpha: float) -> Dict[str, np.ndarray]:
+    """Forward load statistics of one batch, by their definitions:
+      f_e = (1/T) #{tokens that chose e}                 ([MM] section 3.1; [FM] section 3.2)
+      P_e = (1/T) sum_t s_e(x_t), s the layer's scores (softmax over all E, or sigmoid)
+      L_aux = alpha E sum_e f_e P_e
+      max/mean load = max_e c_e / (T k / E), c_e the assignments of expert e ([T26] "Routing
+                     creates an assignment problem": maximum load divided by mean load)."""
+    T, k = idx.shape
+    c = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            c[idx[t, j]] += 1
+    f = c / T
+    P = scores(l32, scoring).mean(axis=0)
+    return {"f": f, "P": P, "aux_loss": aux_loss(f, P, alpha), "max_over_mean": float(c.max() / (T * k / E)),
+            "counts": c}
 
 
 def dispatch_bytes(T: int, k: int, d: int, elem_bytes: int) -> int:

@@ -107,3 +107,81 @@ def test_bias_controller_balances_skewed_layer(moe):
         moe.update_sel_bias(cfg, counts, 0.02, sb)
     assert moe.get_device_error() == 0
     assert history[0] > 3.0 and np.median(history[-50:]) < 1.2, (history[0], history[-50:])
+
+
+# Switch-style gating: softmax over all E, top-k, gates = the probabilities themselves.
+PLAIN_SHAPES = [
+    S("switch_top1_e16", T=300, d=256, d_ff=192, E=16, k=1, dtype="bf16", scoring="softmax_norenorm"),
+    S("plain_top2_e64", T=200, d=192, d_ff=128, E=64, k=2, dtype="bf16", scoring="softmax_norenorm",
+      logit_bias_std=1.0),
+    S("plain_top2_f32", T=64, d=64, d_ff=96, E=8, k=2, dtype="f32", scoring="softmax_norenorm"),
+]
+
+
+@pytest.mark.parametrize("shape", PLAIN_SHAPES, ids=[s.name for s in PLAIN_SHAPES])
+def test_switch_style_gates(moe, shape):
+    s = shape
+    case = Case(s, 0)
+    ref = case.forward()
+    assert np.all(ref["gate"].sum(axis=1) < 1.0)
+    lb = None if case.logit_bias is None else torch.from_numpy(case.logit_bias).cuda()
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    moe.route(cfg, x, Wg, idx, gate, logit_bias=lb, ws=ws)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.max(np.abs(gate.cpu().numpy() - ref["gate"])) <= GATE_ATOL
+    W = upload_experts(s, 0, keep=range(s.E))
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb, topk_idx_out=idx)
+    assert moe.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+
+
+STATS_SHAPES = [
+    S("stats_softmax_e8", T=4096, d=512, d_ff=64, E=8, k=2, dtype="bf16", scoring="softmax"),
+    S("stats_sigmoid_e256", T=1000, d=256, d_ff=64, E=256, k=8, dtype="bf16", scoring="sigmoid",
+      logit_bias_std=1.0),
+    S("stats_skewed_e64", T=777, d=128, d_ff=64, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.5),
+    S("stats_plain_e12_f32", T=50, d=40, d_ff=16, E=12, k=1, dtype="f32", scoring="softmax_norenorm"),
+]
+
+
+@pytest.mark.parametrize("shape", STATS_SHAPES, ids=[s.name for s in STATS_SHAPES])
+def test_load_stats(moe, shape):
+    s = shape
+    case = Case(s, 0)
+    r = case.route()
+    ref = orc.load_stats(r["idx"], r["logits"], s.E, s.scoring, 0.01)
+    lb = None if case.logit_bias is None else torch.from_numpy(case.logit_bias).cuda()
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.empty((s.T * s.k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((s.T * s.k, s.d), dtype=tdtype(s), device="cuda")
+    moe.route(cfg, x, Wg, idx, gate, logit_bias=lb, ws=ws)
+    moe.dispatch(cfg, idx, x, counts, offsets, perm, inv, x_perm, ws)
+    f = torch.empty((s.E,), dtype=torch.float32, device="cuda")
+    P = torch.empty_like(f)
+    summary = torch.empty((2,), dtype=torch.float32, device="cuda")
+    moe.load_stats(cfg, x, Wg, counts, 0.01, f, P, summary, logit_bias=lb, ws=ws)
+    assert moe.last_launch_count() == 3
+    assert moe.get_device_error() == 0
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(f.cpu().numpy(), (ref["counts"].astype(np.float32) / np.float32(s.T)))
+    assert np.allclose(P.cpu().numpy(), ref["P"], rtol=2e-4, atol=1e-7)
+    got = summary.cpu().numpy()
+    assert abs(got[0] - ref["aux_loss"]) <= 2e-4 * ref["aux_loss"]
+    assert abs(got[1] - ref["max_over_mean"]) <= 1e-6 * ref["max_over_mean"]
+    # identical on a second call
+    P2 = torch.empty_like(P)
+    moe.load_stats(cfg, x, Wg, counts, 0.01, f, P2, summary, logit_bias=lb, ws=ws)
+    assert torch.equal(P, P2)

@@ -271,6 +271,45 @@ def check_bias_controller_balances():
     assert start > 2.0 and m < 1.2, (start, m)
 
 
+def check_switch_top1_no_renorm():
+    # Switch: top-1, y = p_i(x) E_i(x) with p the softmax probability itself ([RA] "The router").
+    x, Wg, W = _rand_layer(24, T=5, d=4, d_ff=3, E=4)
+    out = orc.forward(x, Wg, _arrays_fn(W), 4, 1, "softmax_norenorm")
+    l = orc.router_logits(x, Wg).astype(np.float64)
+    for t in range(5):
+        ex = [math.exp(v) for v in l[t]]
+        e = int(np.argmax(l[t]))
+        p = ex[e] / sum(ex)
+        assert out["idx"][t, 0] == e and abs(out["gate"][t, 0] - p) < 1e-12 and p < 1.0
+        ref = p * dense_swiglu_loops(x[t:t + 1], W["W1"][e], W["W2"][e], W["W3"][e])[0]
+        assert np.allclose(out["y"][t], ref, rtol=1e-12, atol=1e-12)
+    # with k = E nothing is left out: the plain and renormalised gates coincide
+    a = orc.route(x, Wg, 4, "softmax_norenorm")
+    b = orc.route(x, Wg, 4, "softmax")
+    assert np.array_equal(a["idx"], b["idx"]) and np.allclose(a["gate"], b["gate"], rtol=1e-12)
+
+
+def check_load_stats():
+    # hand example: E = 4, k = 2, three tokens choosing (0,1), (0,2), (0,3): counts 3,1,1,1,
+    # mean load 6/4 -> max/mean 2; f = counts / T; every token's logits (ln 3, 0, 0, 0) give the
+    # softmax (1/2, 1/6, 1/6, 1/6) = P; L_aux = alpha E sum f P.
+    idx = np.array([[0, 1], [0, 2], [0, 3]], np.int32)
+    l = np.tile(np.array([math.log(3.0), 0, 0, 0], np.float32), (3, 1))
+    st = orc.load_stats(idx, l, 4, "softmax", 0.01)
+    assert st["counts"].tolist() == [3, 1, 1, 1] and st["max_over_mean"] == 2.0
+    assert np.allclose(st["f"], [1.0, 1 / 3, 1 / 3, 1 / 3], rtol=1e-15)
+    assert np.allclose(st["P"], [0.5, 1 / 6, 1 / 6, 1 / 6], rtol=1e-6)
+    assert abs(st["aux_loss"] - 0.01 * 4 * (0.5 + 3 * (1 / 3) * (1 / 6))) < 1e-9
+    # uniform scores with top-1 routing: L_aux = alpha whatever the assignment ([MM] 3.1, E = 64)
+    E, T = 64, 256
+    idx = (np.arange(T) % E).reshape(T, 1).astype(np.int32)
+    st = orc.load_stats(idx, np.zeros((T, E), np.float32), E, "softmax", 0.01)
+    assert abs(st["aux_loss"] - 0.01) < 1e-15 and st["max_over_mean"] == 1.0
+    # sigmoid scores: P is the mean sigmoid score
+    st = orc.load_stats(idx[:2], np.zeros((2, E), np.float32), E, "sigmoid", 1.0)
+    assert np.allclose(st["P"], 0.5, rtol=1e-15)
+
+
 def check_printed_values():
     G = json.load(open(GOLDEN))
     for c in G["combinations"]:
@@ -314,7 +353,7 @@ CHECKS = [check_router_logits_closed_form, check_scores_closed_forms, check_topk
           check_dispatch, check_swiglu_scalar_closed_form, check_swiglu_vs_loops,
           check_E1_k1_is_dense_swiglu, check_grouped_equals_bruteforce, check_shared_only,
           check_selection_bias, check_selection_bias_sigmoid_uses_scores, check_sel_bias_update_closed_form,
-          check_bias_controller_balances, check_printed_values]
+          check_bias_controller_balances, check_switch_top1_no_renorm, check_load_stats, check_printed_values]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -371,6 +410,10 @@ def _bias_on_logits(l32, scoring, sel_bias=None):             # sigmoid bias add
     return orc.__dict__["_orig_selection_keys"](l32, "softmax", sel_bias)
 
 
+def _aux_without_E(f, P, alpha):                               # the factor E left out
+    return float(alpha * np.sum(np.asarray(f) * np.asarray(P)))
+
+
 PLANTS = [
     ("swiglu_expert", _swapped_swiglu, [check_swiglu_scalar_closed_form, check_swiglu_vs_loops]),
     ("gates_from_scores", _no_renorm, [check_gate_invariants, check_gates_two_formulations]),
@@ -381,6 +424,7 @@ PLANTS = [
     ("select_topk", _topk_ascending, [check_topk_bruteforce]),
     ("update_sel_bias", _bias_update_wrong_sign, [check_sel_bias_update_closed_form, check_bias_controller_balances]),
     ("selection_keys", _bias_on_logits, [check_selection_bias_sigmoid_uses_scores]),
+    ("aux_loss", _aux_without_E, [check_load_stats]),
 ]
 
 
