@@ -91,6 +91,12 @@ typedef struct {
   int32_t scoring;     /* moe_scoring */
   int32_t n_shared;    /* always-on shared experts (0 = none) */
   int32_t d_ff_shared; /* shared expert width */
+  /* Capacity factor c (0 = no capacity: nothing is dropped).  With c > 0 every expert has
+     ceil(T*k*c/E) slots and keeps its first pairs in token order; the pairs beyond are dropped
+     and contribute nothing to the output (page "8.6 - Mixture of Experts (MoE)", section 3.2;
+     page "Mixture-of-Experts, from the router to the all-to-all", "Capacity and token
+     dropping").  Finite and >= 0. */
+  float capacity_factor;
 } moe_config;
 
 /* Stages recorded by moe_forward_profiled: route, dispatch, experts (W1/W2 + SwiGLU),
@@ -159,12 +165,15 @@ moe_status moe_update_sel_bias(const moe_config* cfg, const int32_t* counts, flo
      topk_idx [T][k] int32 in (every id in [0, E); an id out of range sets the device
               error word and that pair is skipped)
      x        [T][d] dtype in
-     counts   [E] int32 out: pairs (t, j) routed to each expert
-     offsets  [E+1] int32 out: exclusive prefix sum of counts; offsets[E] = T*k
-     perm_tok [T*k] int32 out: token of the p-th pair in expert order; pairs of one
-              expert keep ascending flattened index t*k + j
-     inv_pos  [T][k] int32 out: position p of pair (t, j)
-     x_perm   [T*k][d] dtype out: x_perm[p] = x[perm_tok[p]]
+     counts   [E] int32 out: pairs (t, j) routed to each expert (its load, before any dropping)
+     offsets  [E+1] int32 out: exclusive prefix sum of the pairs each expert keeps:
+              counts[e], or min(counts[e], slots) with a capacity factor; offsets[E] = pairs
+              kept (T*k without a capacity factor)
+     perm_tok [T*k] int32 out: token of the p-th kept pair in expert order, p < offsets[E];
+              pairs of one expert keep ascending flattened index t*k + j; entries from
+              offsets[E] on are not written
+     inv_pos  [T][k] int32 out: position p of pair (t, j), or -1 if it was dropped
+     x_perm   [T*k][d] dtype out: x_perm[p] = x[perm_tok[p]] for p < offsets[E]
    Deterministic: no atomics; identical inputs give identical outputs. */
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                         int32_t* counts, int32_t* offsets, int32_t* perm_tok,

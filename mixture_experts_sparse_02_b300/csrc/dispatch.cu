@@ -1,6 +1,9 @@
 // Dispatch of the MoE layer: per-expert histogram, exclusive prefix sum, stable permutation
 // and row gather (page "Mixture of Experts: What Actually Happens When a Token Hits the
-// Router", Step 3: sort tokens by assigned expert into contiguous blocks per expert).
+// Router", Step 3: sort tokens by assigned expert into contiguous blocks per expert).  With a
+// capacity of `cap` slots per expert, an expert keeps its first `cap` pairs in token order and
+// the rest are dropped (page "8.6 - Mixture of Experts (MoE)", section 3.2; page "Mixture-of-
+// Experts, from the router to the all-to-all", "Capacity and token dropping").
 //
 // The T*k (token, slot) pairs, in flattened order i = t*k + j, are cut into chunks of 256
 // pairs, one chunk per warp.  No atomics anywhere, so counts, offsets and the permutation are
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(WARPS * 32) hist_kernel(const int32_t* __restr
 // One block of 1024 threads.  Thread (e, s) owns expert e's column of the [n_chunks][E]
 // count matrix over the chunk segment s (S segments per expert).
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts, int n_chunks, int E,
-                                                    int S, int32_t* __restrict__ chunk_base,
+                                                    int S, int cap, int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int part[1024];   // [S][E] segment sums, then exclusive segment bases
   __shared__ int tot[1024];    // per-expert totals, then offsets
@@ -80,8 +83,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
       part[q * E + tid] = run;
       run += v;
     }
-    tot[tid] = run;
-    counts[tid] = run;
+    tot[tid] = min(run, cap);   // pairs the expert keeps; offsets are over kept pairs
+    counts[tid] = run;          // the expert's load, before any dropping
   }
   __syncthreads();
   // exclusive scan of tot[0..E) (E <= 1024) across the block
@@ -124,7 +127,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
 }
 
 __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __restrict__ idx, long long N, int k, int E,
-                                                             int n_chunks, const int32_t* __restrict__ chunk_base,
+                                                             int n_chunks, int cap, const int32_t* __restrict__ chunk_base,
+                                                             const int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ perm_tok,
                                                              int32_t* __restrict__ inv_pos) {
   extern __shared__ int sh[];
@@ -147,8 +151,12 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
     if (i < N) {
       if (e >= 0) {
         const int pos = run[e] + __popc(m & lt);
-        perm_tok[pos] = (int32_t)(i / k);
-        inv_pos[i] = pos;
+        if (pos - __ldg(offsets + e) < cap) {   // rank within the expert, in token order
+          perm_tok[pos] = (int32_t)(i / k);
+          inv_pos[i] = pos;
+        } else {
+          inv_pos[i] = -1;                        // the expert is full: the pair is dropped
+        }
       } else {
         inv_pos[i] = -1;
       }
@@ -161,10 +169,14 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
 
 template <typename V>
 __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, const int32_t* __restrict__ perm_tok,
-                                                     long long rows, int vec_per_row, long long T,
-                                                     V* __restrict__ xp) {
+                                                     long long rows, const int32_t* __restrict__ rows_dev,
+                                                     int vec_per_row, long long T, V* __restrict__ xp) {
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (rows_dev) {   // rows actually kept (offsets[E]); never more than the buffer holds
+    const long long kept = __ldg(rows_dev);
+    rows = kept < rows ? (kept > 0 ? kept : 0) : rows;
+  }
   for (long long p = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; p < rows; p += warps) {
     const int t = __ldg(perm_tok + p);
     V* dst = xp + (size_t)p * vec_per_row;
@@ -178,9 +190,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
 
 int dispatch_num_chunks(long long pairs) { return (int)((pairs + CHUNK - 1) / CHUNK); }
 
-cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32_t* chunk_counts, int32_t* chunk_base,
-                             int32_t* counts, int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint32_t* err,
-                             cudaStream_t st, int* launches) {
+cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int cap, int32_t* chunk_counts,
+                             int32_t* chunk_base, int32_t* counts, int32_t* offsets, int32_t* perm_tok,
+                             int32_t* inv_pos, uint32_t* err, cudaStream_t st, int* launches) {
   const long long N = (long long)T * k;
   const int n_chunks = dispatch_num_chunks(N);
   const unsigned blocks = (unsigned)((n_chunks + WARPS - 1) / WARPS);
@@ -190,29 +202,30 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32
   if (e != cudaSuccess) return e;
   int S = 1;
   while (S * 2 * E <= 1024 && S * 2 <= n_chunks) S *= 2;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, n_chunks, E, S, chunk_base, counts, offsets);
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, n_chunks, E, S, cap, chunk_base, counts, offsets);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, k, E, n_chunks, chunk_base, perm_tok, inv_pos);
+  permute_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, k, E, n_chunks, cap, chunk_base, offsets, perm_tok,
+                                                  inv_pos);
   g_launches += 3;
   if (launches) *launches += 3;
   return cudaGetLastError();
 }
 
-cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, int d, int elem_bytes,
-                        void* x_perm, cudaStream_t st) {
+cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, const int32_t* rows_dev,
+                        int d, int elem_bytes, void* x_perm, cudaStream_t st) {
   const long long row_bytes = (long long)d * elem_bytes;
   const int threads = 256;
   long long want = (rows * 32 + threads - 1) / threads;
   const unsigned blocks = (unsigned)(want < 148LL * 16 ? want : 148LL * 16);
   if (row_bytes % 16 == 0 && ((uintptr_t)x % 16 == 0) && ((uintptr_t)x_perm % 16 == 0)) {
-    gather_kernel<uint4><<<blocks, threads, 0, st>>>((const uint4*)x, perm_tok, rows, (int)(row_bytes / 16), T,
+    gather_kernel<uint4><<<blocks, threads, 0, st>>>((const uint4*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 16), T,
                                                      (uint4*)x_perm);
   } else if (row_bytes % 4 == 0) {
-    gather_kernel<uint32_t><<<blocks, threads, 0, st>>>((const uint32_t*)x, perm_tok, rows, (int)(row_bytes / 4), T,
+    gather_kernel<uint32_t><<<blocks, threads, 0, st>>>((const uint32_t*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 4), T,
                                                         (uint32_t*)x_perm);
   } else {
-    gather_kernel<uint16_t><<<blocks, threads, 0, st>>>((const uint16_t*)x, perm_tok, rows, (int)(row_bytes / 2), T,
+    gather_kernel<uint16_t><<<blocks, threads, 0, st>>>((const uint16_t*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 2), T,
                                                         (uint16_t*)x_perm);
   }
   ++g_launches;

@@ -66,11 +66,15 @@ cudaError_t load_stats(const float* logits, const float* logit_bias, const int32
 
 // ---- dispatch
 int dispatch_num_chunks(long long pairs);
-cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int32_t* chunk_counts,
+// cap: slots per expert (pairs beyond the first cap of an expert, in token order, are dropped:
+// inv_pos = -1); a value >= T*k keeps everything.  counts = loads before dropping, offsets over
+// the kept pairs.
+cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int cap, int32_t* chunk_counts,
                              int32_t* chunk_base, int32_t* counts, int32_t* offsets, int32_t* perm_tok,
                              int32_t* inv_pos, uint32_t* err, cudaStream_t st, int* launches);
-cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, int d, int elem_bytes,
-                        void* x_perm, cudaStream_t st);
+// rows_dev (optional, device): the number of rows to copy, bounded by `rows`.
+cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, const int32_t* rows_dev,
+                        int d, int elem_bytes, void* x_perm, cudaStream_t st);
 
 // ---- combine
 cudaError_t combine(int dtype, const float* y_perm, const int32_t* inv_pos, const float* gate, const float* ys,

@@ -99,6 +99,16 @@ static FwdLayout fwd_layout(const moe_config& c) {
   return L;
 }
 
+// Slots per expert: ceil(T k c / E) for a capacity factor c > 0 (page "8.6 - Mixture of
+// Experts (MoE)", section 3.2: capacity = T k / E * c), computed in double as (T k) * c / E;
+// without a capacity factor, T k (nothing is ever dropped).
+static int capacity_slots(const moe_config& c) {
+  const long long pairs = (long long)c.T * c.k;
+  if (!(c.capacity_factor > 0.0f)) return (int)pairs;
+  const double slots = ceil((double)pairs * (double)c.capacity_factor / (double)c.E);
+  return slots >= (double)pairs ? (int)pairs : (int)slots;
+}
+
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 static bool aligned4(const void* p) { return ((uintptr_t)p & 3) == 0; }
 
@@ -110,6 +120,7 @@ static moe_status check_config(const moe_config* c) {
       c->scoring != MOE_SOFTMAX_TOPK_PLAIN)
     return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || (c->n_shared > 0 && c->d_ff_shared <= 0)) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->capacity_factor) || c->capacity_factor < 0.0f) return MOE_ERR_INVALID_ARG;
   if (c->E > 1024 || c->k > 32) return MOE_ERR_UNSUPPORTED;
   const long long N = (long long)c->T * c->k;
   if (N >= (1LL << 31) - 256) return MOE_ERR_UNSUPPORTED;
@@ -152,9 +163,9 @@ static moe_status stage_route(const moe_config& c, const void* x, const void* W_
 static moe_status stage_dispatch(const moe_config& c, const int32_t* idx, const void* x, int32_t* counts,
                                  int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, int32_t* chunk_counts,
                                  int32_t* chunk_base, cudaStream_t st) {
-  MOE_CUDA(dispatch_indices(idx, c.T, c.k, c.E, chunk_counts, chunk_base, counts, offsets, perm, inv, error_word(), st,
-                            nullptr));
-  return cuda_status(gather_rows(x, c.T, perm, (long long)c.T * c.k, c.d, esize(c), x_perm, st));
+  MOE_CUDA(dispatch_indices(idx, c.T, c.k, c.E, capacity_slots(c), chunk_counts, chunk_base, counts, offsets, perm,
+                            inv, error_word(), st, nullptr));
+  return cuda_status(gather_rows(x, c.T, perm, (long long)c.T * c.k, offsets + c.E, c.d, esize(c), x_perm, st));
 }
 
 static moe_status stage_w12(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* W1,

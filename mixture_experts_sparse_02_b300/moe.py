@@ -32,7 +32,7 @@ class MoEConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scoring", ctypes.c_int32), ("n_shared", ctypes.c_int32),
-                ("d_ff_shared", ctypes.c_int32)]
+                ("d_ff_shared", ctypes.c_int32), ("capacity_factor", ctypes.c_float)]
 
 
 class MoEError(RuntimeError):
@@ -81,15 +81,16 @@ def status_string(status: int) -> str:
 
 
 def config(T: int, d: int, d_ff: int, E: int, k: int, dtype: str = "bf16", scoring: str = "softmax",
-           n_shared: int = 0, d_ff_shared: int = 0) -> MoEConfig:
+           n_shared: int = 0, d_ff_shared: int = 0, capacity_factor: float = 0.0) -> MoEConfig:
     return MoEConfig(T, d, d_ff, E, k, MOE_BF16 if dtype == "bf16" else MOE_F32, SCORING[scoring],
-                     n_shared, d_ff_shared)
+                     n_shared, d_ff_shared, capacity_factor)
 
 
 def config_from_shape(shape, T: Optional[int] = None) -> MoEConfig:
-    """MoEConfig from any object with T, d, d_ff, E, k, dtype, scoring, n_shared, d_ff_shared."""
+    """MoEConfig from any object with T, d, d_ff, E, k, dtype, scoring, n_shared, d_ff_shared
+    (and optionally capacity_factor)."""
     return config(shape.T if T is None else T, shape.d, shape.d_ff, shape.E, shape.k, shape.dtype,
-                  shape.scoring, shape.n_shared, shape.d_ff_shared)
+                  shape.scoring, shape.n_shared, shape.d_ff_shared, getattr(shape, "capacity_factor", 0.0))
 
 
 def _ptr(t) -> Optional[int]:

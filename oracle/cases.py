@@ -84,4 +84,4 @@ class Case:
     def forward(self):
         s = self.shape
         return orc.forward(self.f64(self.x), self.f64(self.W_g), self.get_w, s.E, s.k, s.scoring,
-                           self.logit_bias, self.sel_bias, s.n_shared)
+                           self.logit_bias, self.sel_bias, s.n_shared, s.capacity_factor)

@@ -163,23 +163,40 @@ def update_sel_bias(sel_bias: np.ndarray, counts: np.ndarray, T: int, k: int, ga
 # --------------------------------------------------------------------------------------
 
 
-def dispatch(idx: np.ndarray, E: int) -> Dict[str, np.ndarray]:
+def capacity_slots(T: int, k: int, E: int, factor: float) -> int:
+    """Slots per expert when a capacity factor c is set: ceil(T k c / E) ([MM] section 3.2:
+    capacity = T k / E * c; [RA] "Capacity and token dropping").  Computed in double as
+    (T k) * c / E with c the float32 value the library is given, then rounded up to whole
+    slots."""
+    return int(math.ceil(float(T * k) * float(np.float32(factor)) / float(E)))
+
+
+def dispatch(idx: np.ndarray, E: int, slots: Optional[int] = None) -> Dict[str, np.ndarray]:
     """Group the (token, slot) pairs by expert ([TR] Step 3: sort tokens by assigned expert
     into contiguous blocks).
 
-    counts[e]   = number of pairs routed to expert e
-    offsets[e]  = sum of counts before e; offsets[E] = T k
-    perm_tok[p] = token of the p-th pair in expert order (pairs of one expert keep the order
-                  of their flattened index t k + j)
-    inv_pos[t, j] = position p of pair (t, j)."""
+    counts[e]   = number of pairs routed to expert e (its load, before any dropping)
+    offsets[e]  = sum of the kept pairs of the experts before e; offsets[E] = pairs kept
+    perm_tok[p] = token of the p-th kept pair in expert order (pairs of one expert keep the
+                  order of their flattened index t k + j)
+    inv_pos[t, j] = position p of pair (t, j), or -1 if the pair was dropped.
+
+    With `slots` (a capacity), an expert keeps its first `slots` pairs in token order and
+    drops the rest ([RA] "Capacity and token dropping": a token that finds its expert full
+    is dropped from it)."""
     T, k = idx.shape
     flat = idx.reshape(-1).astype(np.int64)
     counts = np.bincount(flat, minlength=E).astype(np.int32)
-    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    kept = counts if slots is None else np.minimum(counts, slots).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(kept)]).astype(np.int32)
+    full_offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     order = np.argsort(flat, kind="stable")
-    perm_tok = (order // k).astype(np.int32)
-    inv = np.empty(T * k, dtype=np.int32)
-    inv[order] = np.arange(T * k, dtype=np.int32)
+    e_of = flat[order]
+    rank = np.arange(T * k, dtype=np.int64) - full_offsets[e_of]
+    keep = rank < kept[e_of]
+    inv = np.full(T * k, -1, dtype=np.int32)
+    inv[order[keep]] = (offsets[e_of[keep]] + rank[keep]).astype(np.int32)
+    perm_tok = (order[keep] // k).astype(np.int32)
     return {"counts": counts, "offsets": offsets, "perm_tok": perm_tok,
             "inv_pos": inv.reshape(T, k)}
 
@@ -238,22 +255,28 @@ def shared_experts(x64: np.ndarray, get_w: WeightFn, n_shared: int) -> Optional[
 def combine(y_perm64: np.ndarray, inv_pos: np.ndarray, gate64: np.ndarray,
             shared64: Optional[np.ndarray] = None) -> np.ndarray:
     """y[t] = sum_j g[t, j] y_perm[inv_pos[t, j]] (+ shared[t]): scatter the expert outputs
-    back to token order and weight them by the gates ([MM] section 2; [TR] Step 3/4)."""
+    back to token order and weight them by the gates ([MM] section 2; [TR] Step 3/4).  Pairs
+    dropped at dispatch (inv_pos = -1) contribute zero ([MM] section 3.2)."""
     T, k = inv_pos.shape
     y = np.zeros((T, y_perm64.shape[1]), np.float64)
     for j in range(k):
-        y += gate64[:, j:j + 1] * y_perm64[inv_pos[:, j]]
+        kept = inv_pos[:, j] >= 0                 # a dropped pair contributes nothing
+        y[kept] += gate64[kept, j:j + 1] * y_perm64[inv_pos[kept, j]]
     if shared64 is not None:
         y += shared64
     return y
 
 
 def forward(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, k: int,
-            scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0) -> Dict[str, np.ndarray]:
-    """The whole layer, evaluated the grouped way: route, dispatch, one SwiGLU per expert
-    over its block, combine (+ shared experts).  All results are returned for comparison."""
+            scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0,
+            capacity_factor: float = 0.0) -> Dict[str, np.ndarray]:
+    """The whole layer, evaluated the grouped way: route, dispatch (with capacity_slots per
+    expert when capacity_factor > 0), one SwiGLU per expert over its block, combine (+ shared
+    experts).  All results are returned for comparison."""
     r = route(x64, Wg64, k, scoring, logit_bias, sel_bias)
-    dsp = dispatch(r["idx"], E)
+    T = x64.shape[0]
+    slots = capacity_slots(T, k, E, capacity_factor) if capacity_factor > 0 else None
+    dsp = dispatch(r["idx"], E, slots)
     x_perm = x64[dsp["perm_tok"]]
     y_perm = experts_grouped(x_perm, dsp["offsets"], get_w)
     ys = shared_experts(x64, get_w, n_shared)
@@ -265,14 +288,20 @@ def forward(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, k: int,
 
 
 def forward_tokens(x_rows64: np.ndarray, idx_rows: np.ndarray, gate_rows: np.ndarray,
-                   get_w: WeightFn, n_shared: int = 0) -> np.ndarray:
+                   get_w: WeightFn, n_shared: int = 0, kept_rows: Optional[np.ndarray] = None) -> np.ndarray:
     """The layer output for a few tokens, given their routing, by the definition
     MoE(x) = sum_j g_j f_{I_j}(x) (+ shared): each chosen expert evaluated on the token
-    itself ([MM] section 2).  Tokens that share an expert are evaluated together."""
+    itself ([MM] section 2).  Tokens that share an expert are evaluated together.  kept_rows
+    [n, k] bool, if given, leaves out the pairs dropped at dispatch."""
     n, k = idx_rows.shape
     y = np.zeros((n, x_rows64.shape[1]), np.float64)
     for e in np.unique(idx_rows):
-        rows, slots = np.nonzero(idx_rows == e)
+        sel = idx_rows == e
+        if kept_rows is not None:
+            sel = sel & kept_rows
+        rows, slots = np.nonzero(sel)
+        if rows.size == 0:
+            continue
         fe = swiglu_expert(x_rows64[rows], get_w("W1", int(e)), get_w("W2", int(e)), get_w("W3", int(e)))
         y[rows] += gate_rows[rows, slots][:, None] * fe
     ys = shared_experts(x_rows64, get_w, n_shared)
@@ -280,17 +309,25 @@ def forward_tokens(x_rows64: np.ndarray, idx_rows: np.ndarray, gate_rows: np.nda
 
 
 def forward_bruteforce(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, k: int,
-                       scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0) -> np.ndarray:
+                       scoring: str, logit_bias=None, sel_bias=None, n_shared: int = 0,
+                       capacity_factor: float = 0.0) -> np.ndarray:
     """The naive evaluation ([TR] Step 3): loop over experts, mask the tokens that chose
     each, run the expert on them, weight by the gate and accumulate.  No sort, no offsets,
-    no permutation: an independent evaluation of the same sum, for tiny inputs."""
+    no permutation: an independent evaluation of the same sum, for tiny inputs.  With a
+    capacity, an expert takes the tokens that chose it in token order and skips the rest
+    once it is full ([RA] "Capacity and token dropping")."""
     r = route(x64, Wg64, k, scoring, logit_bias, sel_bias)
     T = x64.shape[0]
+    slots = capacity_slots(T, k, E, capacity_factor) if capacity_factor > 0 else None
     y = np.zeros_like(x64, dtype=np.float64)
     for e in range(E):
+        taken = 0
         for t in range(T):
             for j in range(k):
                 if r["idx"][t, j] == e:
+                    if slots is not None and taken >= slots:
+                        continue
+                    taken += 1
                     f = swiglu_expert(x64[t:t + 1], get_w("W1", e), get_w("W2", e), get_w("W3", e))[0]
                     y[t] += r["gate"][t, j] * f
     ys = shared_experts(x64, get_w, n_shared)

@@ -84,6 +84,8 @@ def test_argument_errors(moe):
     bad_cfg = moe.config(16, 64, 64, 8, 2)
     bad_cfg.scoring = 5
     assert _fwd(moe, bad_cfg) == moe.MOE_ERR_INVALID_ARG
+    for cf in (-1.0, float("nan"), float("inf")):
+        assert _fwd(moe, moe.config(16, 64, 64, 8, 2, capacity_factor=cf)) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_empty_batch_launches_nothing(moe):

@@ -1,0 +1,127 @@
+"""GPU parity for the capacity factor and token dropping: each expert keeps its first
+ceil(T k c / E) assignments in token order and drops the rest, which then contribute nothing.
+
+Pages: "8.6 - Mixture of Experts (MoE)", section 3.2; "Mixture-of-Experts, from the router to
+the all-to-all", "Capacity and token dropping".
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import Case
+from oracle import moe_oracle as orc
+
+from gpu_util import (dev_to_f64, from_dev_stored, layer_out_err, max_rel_err, require_cuda, tdtype, to_dev,
+                      upload_experts, y_tol)
+
+pytestmark = pytest.mark.gpu
+
+S = wl.MoEShape
+CAP_SHAPES = [
+    # skewed loads, about 40% of the pairs dropped.  (With d_ff = 128 and a bias of std 1.5 the
+    # outputs reach 13.5 x rms and the bf16 rounding of h alone gives 2.9% of rms: outside
+    # the 2e-2 rms rule for any bf16 evaluation, so that shape is not used.)
+    S("cap_skewed_e64", T=512, d=256, d_ff=256, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.0,
+      capacity_factor=1.25),
+    S("cap_e8_k2", T=1000, d=256, d_ff=192, E=8, k=2, dtype="bf16", scoring="softmax", logit_bias_std=0.7,
+      capacity_factor=1.25),
+    S("cap_sigmoid_shared", T=300, d=192, d_ff=128, E=32, k=4, dtype="bf16", scoring="sigmoid", n_shared=1,
+      d_ff_shared=64, logit_bias_std=1.0, capacity_factor=0.5),
+    S("cap_f32", T=90, d=64, d_ff=48, E=6, k=2, dtype="f32", scoring="softmax", logit_bias_std=1.0,
+      capacity_factor=1.0),
+]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return require_cuda()
+
+
+def _dispatch_buffers(s):
+    z = lambda *shape: torch.full(shape, -7, dtype=torch.int32, device="cuda")
+    return dict(counts=z(s.E), offsets=z(s.E + 1), perm=z(s.T * s.k), inv=z(s.T, s.k),
+                x_perm=torch.zeros((s.T * s.k, s.d), dtype=tdtype(s), device="cuda"))
+
+
+@pytest.mark.parametrize("shape", CAP_SHAPES, ids=[s.name for s in CAP_SHAPES])
+def test_forward_with_capacity(moe, shape):
+    s = shape
+    case = Case(s, 0)
+    ref = case.forward()
+    dropped = int((ref["inv_pos"] == -1).sum())
+    assert dropped > 0
+    W = upload_experts(s, 0, keep=range(s.E))
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    lb = None if case.logit_bias is None else torch.from_numpy(case.logit_bias).cuda()
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb, Ws1=W.get("Ws1"), Ws2=W.get("Ws2"),
+                Ws3=W.get("Ws3"), topk_idx_out=idx, counts_out=counts)
+    assert moe.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    # the same layer without a capacity differs exactly where pairs were dropped
+    nocap = orc.forward(case.f64(case.x), case.f64(case.W_g), case.get_w, s.E, s.k, s.scoring, case.logit_bias,
+                        None, s.n_shared)
+    hit = (ref["inv_pos"] == -1).any(axis=1)
+    assert np.allclose(ref["y"][~hit], nocap["y"][~hit], rtol=1e-12, atol=1e-12)
+    assert not np.allclose(ref["y"][hit], nocap["y"][hit])
+
+
+@pytest.mark.parametrize("shape", CAP_SHAPES, ids=[s.name for s in CAP_SHAPES])
+def test_dispatch_and_experts_with_capacity(moe, shape):
+    s = shape
+    case = Case(s, 0)
+    r = case.route()
+    slots = orc.capacity_slots(s.T, s.k, s.E, s.capacity_factor)
+    ref = orc.dispatch(r["idx"], s.E, slots)
+    kept = int(ref["offsets"][-1])
+    assert kept < s.T * s.k
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    x = to_dev(case.x, s)
+    idx = torch.from_numpy(r["idx"]).cuda()
+    for call in ("dispatch", "dispatch_static"):
+        b = _dispatch_buffers(s)
+        if call == "dispatch":
+            moe.dispatch(cfg, idx, x, b["counts"], b["offsets"], b["perm"], b["inv"], b["x_perm"], ws)
+        else:
+            moe.dispatch_static(cfg, idx, x, b["counts"], b["offsets"], b["perm"], b["inv"], b["x_perm"])
+        assert np.array_equal(b["counts"].cpu().numpy(), ref["counts"]), call
+        assert np.array_equal(b["offsets"].cpu().numpy(), ref["offsets"]), call
+        assert np.array_equal(b["perm"][:kept].cpu().numpy(), ref["perm_tok"]), call
+        assert np.array_equal(b["inv"].cpu().numpy(), ref["inv_pos"]), call
+        assert np.array_equal(from_dev_stored(b["x_perm"][:kept], s), case.x[ref["perm_tok"]]), call
+        assert int((b["perm"][kept:] == -7).sum()) == s.T * s.k - kept      # nothing written past the kept pairs
+    # experts over the kept blocks only
+    W = upload_experts(s, 0, keep=range(s.E))
+    x_perm = to_dev(case.x[ref["perm_tok"]], s)
+    x_full = torch.zeros((s.T * s.k, s.d), dtype=tdtype(s), device="cuda")
+    x_full[:kept] = x_perm
+    y_perm = torch.full((s.T * s.k, s.d), 123.0, dtype=torch.float32, device="cuda")
+    moe.experts(cfg, x_full, torch.from_numpy(ref["offsets"]).cuda(), W["W1"], W["W2"], W["W3"], y_perm, ws)
+    assert moe.get_device_error() == 0
+    y_ref = orc.experts_grouped(case.f64(case.x[ref["perm_tok"]]), ref["offsets"], case.get_w)
+    assert max_rel_err(dev_to_f64(y_perm[:kept]), y_ref) <= y_tol(s)
+    assert bool((y_perm[kept:] == 123.0).all())                           # rows past the kept pairs untouched
+
+
+def test_capacity_nobody_reaches_changes_nothing(moe):
+    s = CAP_SHAPES[1].replace(capacity_factor=0.0)
+    case = Case(s, 0)
+    W = upload_experts(s, 0)
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    lb = torch.from_numpy(case.logit_bias).cuda()
+    out = []
+    for c in (0.0, 100.0):
+        cfg = moe.config_from_shape(s.replace(capacity_factor=c))
+        ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+        y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+        moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb)
+        out.append(y)
+    assert torch.equal(out[0], out[1])

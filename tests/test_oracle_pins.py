@@ -310,6 +310,55 @@ def check_load_stats():
     assert np.allclose(st["P"], 0.5, rtol=1e-15)
 
 
+def check_capacity_dropping():
+    # The printed example ([RA] "Capacity and token dropping"): 4,096 tokens, 64 experts,
+    # top-8, capacity factor 1.0 -> 512 slots; an expert picked 600 times drops 88, and the
+    # 88 dropped are its last 88 tokens in token order.
+    T, E, k = 4096, 64, 8
+    assert orc.capacity_slots(T, k, E, 1.0) == 512
+    r = _rng(25)
+    idx = np.empty((T, k), np.int32)
+    hot = set(r.choice(T, 600, replace=False).tolist())
+    others = np.array([e for e in range(E) if e != 7])
+    for t in range(T):
+        pick = r.choice(others, k - 1 if t in hot else k, replace=False).tolist()
+        idx[t] = ([7] + pick) if t in hot else pick
+    d = orc.dispatch(idx, E, 512)
+    assert d["counts"][7] == 600
+    kept7 = d["offsets"][8] - d["offsets"][7]
+    assert kept7 == 512 and d["counts"][7] - kept7 == 88
+    hot_sorted = sorted(hot)
+    assert all(d["inv_pos"][t, 0] >= 0 for t in hot_sorted[:512])
+    assert all(d["inv_pos"][t, 0] == -1 for t in hot_sorted[512:])
+    kept = np.minimum(d["counts"], 512)
+    assert int((d["inv_pos"] == -1).sum()) == int((d["counts"] - kept).sum())
+    assert d["offsets"][-1] == kept.sum() == len(d["perm_tok"])
+    # positions of kept pairs are a bijection onto 0 .. kept - 1, and point back to their token
+    flat = d["inv_pos"].reshape(-1)
+    live = flat[flat >= 0]
+    assert sorted(live.tolist()) == list(range(int(kept.sum())))
+    tok = np.repeat(np.arange(T), k)[flat >= 0]
+    assert np.array_equal(d["perm_tok"][live], tok)
+    # slots in whole numbers: ceil(T k c / E)
+    assert orc.capacity_slots(10, 2, 3, 1.0) == 7 and orc.capacity_slots(8, 1, 4, 1.25) == 3
+
+
+def check_capacity_grouped_equals_bruteforce():
+    # Dropped pairs contribute nothing: the grouped evaluation with a capacity equals the
+    # naive per-expert loop that skips a token once its expert is full.
+    x, Wg, W = _rand_layer(26, T=24, d=6, d_ff=5, E=4)
+    Wg[:, 1] += 0.8                     # skew towards expert 1 so that it overflows
+    for c in (0.5, 1.0, 1.25):
+        g = orc.forward(x, Wg, _arrays_fn(W), 4, 2, "softmax", capacity_factor=c)
+        b = orc.forward_bruteforce(x, Wg, _arrays_fn(W), 4, 2, "softmax", capacity_factor=c)
+        assert np.allclose(g["y"], b, rtol=1e-12, atol=1e-12)
+        assert (g["inv_pos"] == -1).any()
+    # a capacity no expert reaches changes nothing
+    g = orc.forward(x, Wg, _arrays_fn(W), 4, 2, "softmax", capacity_factor=100.0)
+    n = orc.forward(x, Wg, _arrays_fn(W), 4, 2, "softmax")
+    assert np.array_equal(g["y"], n["y"]) and np.array_equal(g["inv_pos"], n["inv_pos"])
+
+
 def check_printed_values():
     G = json.load(open(GOLDEN))
     for c in G["combinations"]:
@@ -353,7 +402,8 @@ CHECKS = [check_router_logits_closed_form, check_scores_closed_forms, check_topk
           check_dispatch, check_swiglu_scalar_closed_form, check_swiglu_vs_loops,
           check_E1_k1_is_dense_swiglu, check_grouped_equals_bruteforce, check_shared_only,
           check_selection_bias, check_selection_bias_sigmoid_uses_scores, check_sel_bias_update_closed_form,
-          check_bias_controller_balances, check_switch_top1_no_renorm, check_load_stats, check_printed_values]
+          check_bias_controller_balances, check_switch_top1_no_renorm, check_load_stats,
+          check_capacity_dropping, check_capacity_grouped_equals_bruteforce, check_printed_values]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -414,6 +464,15 @@ def _aux_without_E(f, P, alpha):                               # the factor E le
     return float(alpha * np.sum(np.asarray(f) * np.asarray(P)))
 
 
+def _drop_earliest(idx, E, slots=None):                       # an expert keeps its LAST pairs
+    if slots is None:
+        return orc.__dict__["_orig_dispatch"](idx, E)
+    rev = orc.__dict__["_orig_dispatch"](idx[::-1].copy(), E, slots)
+    T, k = idx.shape
+    inv = rev["inv_pos"][::-1].copy()
+    return {"counts": rev["counts"], "offsets": rev["offsets"], "perm_tok": rev["perm_tok"], "inv_pos": inv}
+
+
 PLANTS = [
     ("swiglu_expert", _swapped_swiglu, [check_swiglu_scalar_closed_form, check_swiglu_vs_loops]),
     ("gates_from_scores", _no_renorm, [check_gate_invariants, check_gates_two_formulations]),
@@ -425,6 +484,7 @@ PLANTS = [
     ("update_sel_bias", _bias_update_wrong_sign, [check_sel_bias_update_closed_form, check_bias_controller_balances]),
     ("selection_keys", _bias_on_logits, [check_selection_bias_sigmoid_uses_scores]),
     ("aux_loss", _aux_without_E, [check_load_stats]),
+    ("dispatch", _drop_earliest, [check_capacity_dropping, check_capacity_grouped_equals_bruteforce]),
 ]
 
 

@@ -45,6 +45,7 @@ class MoEShape:
     n_shared: int = 0
     d_ff_shared: int = 0
     logit_bias_std: float = 0.0   # > 0: a per-expert bias added to the logits
+    capacity_factor: float = 0.0  # > 0: each expert keeps at most ceil(T k c / E) assignments
 
     def replace(self, **kw) -> "MoEShape":
         return dataclasses.replace(self, **kw)
