@@ -39,9 +39,10 @@ DECODE_WORKLOAD = "mixtral_decode"
 FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM on the default workload, from
-# one ncu capture (profiles/), valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"source_sha256": "586062c6d25a549d7593ea7e673c47abf12cc2bff9a02476b4c1642616cf4fe1",
-               "bytes_per_launch": 2169.6e6}
+# one ncu capture of a half-size case scaled to the full launch (profiles/), per kernel
+# variant, valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {"source_sha256": "25f7aeaa4f5461994945df46e3fe2596650a2466da3f5d93124ca6efb2c5eada",
+               "bytes_per_launch": {"pair": 2206.4e6}}
 
 
 def _sha256(path):
@@ -234,11 +235,21 @@ def to_dev(torch, a, shape):
     return t.cuda()
 
 
-def traffic_for_kernel():
+def traffic_for_kernel(variant):
     src = os.path.join(ROOT, "mixture_experts_sparse_02_b300", "csrc", "gemm_tc.cu")
     if NCU_TRAFFIC["source_sha256"] and os.path.exists(src) and _sha256(src) == NCU_TRAFFIC["source_sha256"]:
-        return NCU_TRAFFIC["bytes_per_launch"]
+        return NCU_TRAFFIC["bytes_per_launch"].get(variant)
     return None
+
+
+def gemm_variant(shape):
+    """Which grouped-GEMM kernel the library runs for the routed experts of this workload:
+    the same rule as the library (CTA pairs when groups average >= 512 rows, unless
+    MOE_GEMM_KERNEL forces one)."""
+    forced = os.environ.get("MOE_GEMM_KERNEL")
+    if forced in ("single", "pair"):
+        return forced
+    return "pair" if shape.T * shape.k >= 512 * shape.E else "single"
 
 
 def run_ours(args, shape, world, rank, local):
@@ -306,9 +317,12 @@ def run_ours(args, shape, world, rank, local):
     t_sh = mean_stage[4] / 1e3
     peak = pk["bf16_tflops"]
     ach = fl_w12 / t_w12 / 1e12
-    roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<EPI_SWIGLU> (W1/W2 + SiLU*mul)",
+    variant = gemm_variant(shape)
+    kname = "grouped_gemm_pair_kernel<EPI_SWIGLU>" if variant == "pair" else "grouped_gemm_kernel<EPI_SWIGLU>"
+    roof = {"bound": "tensor", "kernel": kname + " (W1/W2 + SiLU*mul)",
             "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-            "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(),
+            "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(variant),
+            "traffic_unit": "bytes per launch (dram read + write)",
             "algorithmic_flops_per_launch": fl_w12}
     eg_t = t_w12 + t_w3 + t_sh
     expert_tflops = (fl_w12 + fl_w3 + fl_sh) / eg_t / 1e12
