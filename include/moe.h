@@ -78,7 +78,16 @@ typedef enum {
   /* softmax over all E, top-k, gates = the softmax probabilities themselves, not
      renormalised; with k = 1 this is the Switch Transformer's y = p_i(x) E_i(x) (page
      "Mixture-of-Experts, from the router to the all-to-all", section "The router") */
-  MOE_SOFTMAX_TOPK_PLAIN = 2
+  MOE_SOFTMAX_TOPK_PLAIN = 2,
+  /* expert choice: softmax over the E experts of each token's logits; every expert takes the
+     m tokens with the largest score for it, m = ceil(T*k*c/E) (c = capacity_factor, 1 when
+     0; at most T), and weights its output for token t by that score; a token may be taken by
+     any number of experts (page "Mixture-of-Experts Internals: A Systems Engineer's Field
+     Manual", section 5.1; page "Mixture-of-Experts, from the router to the all-to-all", "Load
+     balancing").  k is the average number of experts per token.  moe_forward,
+     moe_route_expert_choice, moe_experts and moe_combine_expert_choice take it; moe_route,
+     moe_dispatch, moe_dispatch_static and moe_combine return MOE_ERR_UNSUPPORTED for it. */
+  MOE_EXPERT_CHOICE = 3
 } moe_scoring;
 
 typedef struct {
@@ -184,8 +193,9 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
    y_perm = ((X W1_e) * SiLU(X W2_e)) W3_e.  Page "8.6 - Mixture of Experts (MoE)",
    section 2 (SwiGLU expert); page "Mixture-of-Experts, from the router to the all-to-all",
    section "Expert parallelism and the all-to-all" (one grouped matrix multiply per expert).
-     x_perm  [T*k][d] dtype   offsets [E+1] int32 (non-decreasing, offsets[0] = 0,
-             offsets[E] = T*k; as written by moe_dispatch)
+     x_perm  [T*k][d] dtype ([E*m][d] under expert choice)   offsets [E+1] int32
+             (non-decreasing, offsets[0] = 0, offsets[E] <= the rows of x_perm; as written by
+             moe_dispatch or moe_route_expert_choice)
      W1, W2  [E][d][d_ff] dtype     W3 [E][d_ff][d] dtype
      y_perm  [T*k][d] float32 out
    The intermediate h = (X W1) * SiLU(X W2) is kept in ws in dtype (bfloat16 for the
@@ -207,10 +217,36 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
                        const void* Ws2, const void* Ws3, void* y, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* Expert-choice route (cfg->scoring == MOE_EXPERT_CHOICE): logits -> per-token softmax ->
+   every expert's m tokens, m = ceil(T*k*c/E) as described at MOE_EXPERT_CHOICE.  Each expert
+   takes the m tokens with the largest float32 score; equal scores go to the lower token id.
+     x [T][d], W_g [d][E], logit_bias [E] or NULL: as for moe_route
+     offsets  [E+1] int32 out: e*m (every expert exactly m rows)
+     perm_tok [E*m] int32 out: expert e's tokens at e*m .. e*m+m-1, in ascending token order
+     gate     [E*m] float32 out: the score s[t][e] of the token at each position
+     pos_of   [T][E] int32 out: the position of (t, e), or -1 if expert e did not take t
+   ws: T*E*4 bytes (the scores).  Limits: T <= 51200 (an expert's T scores sit in shared
+   memory); for float32 layers d must be a multiple of 4.  Then gather x rows with perm_tok
+   (x_perm[p] = x[perm_tok[p]]), run moe_experts with offsets, and combine. */
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const void* W_g, const float* logit_bias,
+                                   int32_t* offsets, int32_t* perm_tok, float* gate, int32_t* pos_of, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
+/* Expert-choice combine: y[t] = sum over the experts e that took t, in expert order, of
+   gate[p] * y_perm[p] with p = pos_of[t][e], summed in float32 and rounded once to dtype
+   (+ the shared experts as in moe_combine).  A token no expert took gets only the shared
+   experts (0 without them).
+     y_perm [E*m][d] float32 (moe_experts output)   gate [E*m]   pos_of [T][E] */
+moe_status moe_combine_expert_choice(const moe_config* cfg, const float* y_perm, const float* gate,
+                                     const int32_t* pos_of, const void* x, const void* Ws1, const void* Ws2,
+                                     const void* Ws3, void* y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The whole layer: route -> dispatch -> experts -> combine (+ shared experts), on one
    stream, with every intermediate in ws.  Page "8.6 - Mixture of Experts (MoE)", section 2
    (MoE(x) = sum over TopK of g_e(x) f_e(x)) and section 4.1 (plus f_shared(x)).
-   topk_idx_out [T][k] int32 and counts_out [E] int32 are optional copies of the routing. */
+   topk_idx_out [T][k] int32 and counts_out [E] int32 are optional copies of the routing.
+   With MOE_EXPERT_CHOICE the layer runs expert-choice routing (route, gather, experts,
+   combine as above); sel_bias, topk_idx_out and counts_out must then be NULL. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g,
                        const float* logit_bias, const float* sel_bias, const void* W1,
                        const void* W2, const void* W3, const void* Ws1, const void* Ws2,

@@ -37,6 +37,33 @@ static size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
 static int esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 
+// Slots per expert: ceil(T k c / E) for a capacity factor c > 0 (page "8.6 - Mixture of
+// Experts (MoE)", section 3.2: capacity = T k / E * c), computed in double as (T k) * c / E;
+// without a capacity factor, T k (nothing is ever dropped).
+static int capacity_slots(const moe_config& c) {
+  const long long pairs = (long long)c.T * c.k;
+  if (!(c.capacity_factor > 0.0f)) return (int)pairs;
+  const double slots = ceil((double)pairs * (double)c.capacity_factor / (double)c.E);
+  return slots >= (double)pairs ? (int)pairs : (int)slots;
+}
+
+// Expert choice: tokens each expert takes, m = ceil(T k c / E) (c = capacity factor, 1 when
+// none is set), at most T (page "Mixture-of-Experts Internals: A Systems Engineer's Field
+// Manual", section 5.1).
+static bool expert_choice(const moe_config& c) { return c.scoring == MOE_EXPERT_CHOICE; }
+
+static int ec_slots(const moe_config& c) {
+  const long long pairs = (long long)c.T * c.k;
+  const double f = c.capacity_factor > 0.0f ? (double)c.capacity_factor : 1.0;
+  const double m = ceil((double)pairs * f / (double)c.E);
+  return m >= (double)c.T ? c.T : (int)m;
+}
+
+// Rows of the permuted activations: the (token, expert) pairs (T k), or E m under expert choice.
+static long long pairs_of(const moe_config& c) {
+  return expert_choice(c) ? (long long)c.E * ec_slots(c) : (long long)c.T * c.k;
+}
+
 // Bytes of each scratch region.
 struct Sizes {
   size_t logits, idx, gate, counts, offsets, chunk, perm, inv, x_perm, h, y_perm, hs, ys, x_io, y_io;
@@ -45,15 +72,15 @@ struct Sizes {
 
 static Sizes sizes(const moe_config& c) {
   Sizes s{};
-  const size_t T = (size_t)c.T, N = T * (size_t)c.k;
-  s.logits = c.E > 32 ? align_up(T * c.E * 4) : 0;
+  const size_t T = (size_t)c.T, N = (size_t)pairs_of(c);
+  s.logits = (c.E > 32 || expert_choice(c)) ? align_up(T * c.E * 4) : 0;
   s.idx = align_up(N * 4);
   s.gate = align_up(N * 4);
   s.counts = align_up((size_t)c.E * 4);
   s.offsets = align_up(((size_t)c.E + 1) * 4);
   s.chunk = 2 * align_up((size_t)dispatch_num_chunks((long long)N) * c.E * 4);
   s.perm = align_up(N * 4);
-  s.inv = align_up(N * 4);
+  s.inv = expert_choice(c) ? align_up(T * c.E * 4) : align_up(N * 4);   // inv_pos, or pos_of [T][E]
   s.x_perm = align_up(N * c.d * esize(c));
   s.h = align_up(N * c.d_ff * esize(c));
   s.y_perm = align_up(N * c.d * 4);
@@ -99,16 +126,6 @@ static FwdLayout fwd_layout(const moe_config& c) {
   return L;
 }
 
-// Slots per expert: ceil(T k c / E) for a capacity factor c > 0 (page "8.6 - Mixture of
-// Experts (MoE)", section 3.2: capacity = T k / E * c), computed in double as (T k) * c / E;
-// without a capacity factor, T k (nothing is ever dropped).
-static int capacity_slots(const moe_config& c) {
-  const long long pairs = (long long)c.T * c.k;
-  if (!(c.capacity_factor > 0.0f)) return (int)pairs;
-  const double slots = ceil((double)pairs * (double)c.capacity_factor / (double)c.E);
-  return slots >= (double)pairs ? (int)pairs : (int)slots;
-}
-
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 static bool aligned4(const void* p) { return ((uintptr_t)p & 3) == 0; }
 
@@ -117,13 +134,20 @@ static moe_status check_config(const moe_config* c) {
   if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0 || c->k > c->E) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->scoring != MOE_SOFTMAX_TOPK_RENORM && c->scoring != MOE_SIGMOID_TOPK_NORM &&
-      c->scoring != MOE_SOFTMAX_TOPK_PLAIN)
+      c->scoring != MOE_SOFTMAX_TOPK_PLAIN && c->scoring != MOE_EXPERT_CHOICE)
     return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || (c->n_shared > 0 && c->d_ff_shared <= 0)) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->capacity_factor) || c->capacity_factor < 0.0f) return MOE_ERR_INVALID_ARG;
-  if (c->E > 1024 || c->k > 32) return MOE_ERR_UNSUPPORTED;
-  const long long N = (long long)c->T * c->k;
-  if (N >= (1LL << 31) - 256) return MOE_ERR_UNSUPPORTED;
+  if (c->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c->scoring == MOE_EXPERT_CHOICE) {
+    // one block per expert holds the T scores of its column in shared memory
+    if ((size_t)c->T * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+    if (c->dtype == MOE_F32 && c->d % 4) return MOE_ERR_UNSUPPORTED;
+  } else if (c->k > 32) {
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const long long N = pairs_of(*c);
+  if (N >= (1LL << 31) - 256 || (long long)c->T * c->k >= (1LL << 31) - 256) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_BF16) {
     if (c->d % 8 || c->d_ff % 8) return MOE_ERR_UNSUPPORTED;
     if (c->n_shared > 0 && c->d_ff_shared % 8) return MOE_ERR_UNSUPPORTED;
@@ -146,18 +170,29 @@ static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 
 // ---------------------------------------------------------------- stages (checked inputs)
 
+// Router logits [T][E] float32 (no bias): tensor cores for bf16 when E is a multiple of 8,
+// CUDA cores otherwise.
+static moe_status router_logits(const moe_config& c, const void* x, const void* W_g, float* logits, cudaStream_t st) {
+  if (c.dtype == MOE_BF16 && c.E % 8 == 0 && aligned16(W_g))
+    return cuda_status(tc_matmul_f32(x, c.T, c.d, W_g, 1, c.E, nullptr, 1, c.T, 0, logits, c.E, 0, error_word(), st));
+  return cuda_status(route_logits_simt(c.dtype, x, W_g, c.T, c.d, c.E, logits, st));
+}
+
 static moe_status stage_route(const moe_config& c, const void* x, const void* W_g, const float* lb, const float* sb,
                               int32_t* idx, float* gate, float* logits, cudaStream_t st) {
   uint32_t* err = error_word();
   if (c.E <= 32) {
     return cuda_status(route_fused(c.dtype, x, W_g, lb, sb, c.T, c.d, c.E, c.k, c.scoring, idx, gate, err, st));
   }
-  if (c.dtype == MOE_BF16 && c.E % 8 == 0 && aligned16(W_g)) {
-    MOE_CUDA(tc_matmul_f32(x, c.T, c.d, W_g, 1, c.E, nullptr, 1, c.T, 0, logits, c.E, 0, err, st));
-  } else {
-    MOE_CUDA(route_logits_simt(c.dtype, x, W_g, c.T, c.d, c.E, logits, st));
-  }
+  MOE_TRY(router_logits(c, x, W_g, logits, st));
   return cuda_status(route_topk(logits, lb, sb, c.T, c.E, c.k, c.scoring, idx, gate, err, st));
+}
+
+// Expert choice: logits -> per-token softmax (in place in `scores`) -> every expert's m tokens.
+static moe_status stage_route_ec(const moe_config& c, const void* x, const void* W_g, const float* lb, float* scores,
+                                 int32_t* offsets, int32_t* perm, float* gate, int32_t* pos_of, cudaStream_t st) {
+  MOE_TRY(router_logits(c, x, W_g, scores, st));
+  return cuda_status(ec_route(scores, lb, c.T, c.E, ec_slots(c), offsets, perm, gate, pos_of, st));
 }
 
 static moe_status stage_dispatch(const moe_config& c, const int32_t* idx, const void* x, int32_t* counts,
@@ -165,12 +200,12 @@ static moe_status stage_dispatch(const moe_config& c, const int32_t* idx, const 
                                  int32_t* chunk_base, cudaStream_t st) {
   MOE_CUDA(dispatch_indices(idx, c.T, c.k, c.E, capacity_slots(c), chunk_counts, chunk_base, counts, offsets, perm,
                             inv, error_word(), st, nullptr));
-  return cuda_status(gather_rows(x, c.T, perm, (long long)c.T * c.k, offsets + c.E, c.d, esize(c), x_perm, st));
+  return cuda_status(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, st));
 }
 
 static moe_status stage_w12(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* W1,
                             const void* W2, void* h, cudaStream_t st) {
-  const long long N = (long long)c.T * c.k;
+  const long long N = pairs_of(c);
   if (c.dtype == MOE_BF16)
     return cuda_status(tc_swiglu(x_perm, N, c.d, W1, W2, c.E, c.d_ff, offsets, c.E, 0, 0, h, error_word(), st));
   return cuda_status(simt_swiglu_f32((const float*)x_perm, (int)N, c.d, (const float*)W1, (const float*)W2, c.d_ff,
@@ -179,7 +214,7 @@ static moe_status stage_w12(const moe_config& c, const void* x_perm, const int32
 
 static moe_status stage_w3(const moe_config& c, const void* h, const int32_t* offsets, const void* W3, float* y_perm,
                            cudaStream_t st) {
-  const long long N = (long long)c.T * c.k;
+  const long long N = pairs_of(c);
   if (c.dtype == MOE_BF16)
     return cuda_status(tc_matmul_f32(h, N, c.d_ff, W3, c.E, c.d, offsets, c.E, 0, 0, y_perm, c.d, 0, error_word(), st));
   return cuda_status(simt_matmul_f32((const float*)h, (int)N, c.d_ff, (const float*)W3, c.d, offsets, c.E, 0,
@@ -208,6 +243,11 @@ static moe_status stage_combine(const moe_config& c, const float* y_perm, const 
   return cuda_status(combine(c.dtype, y_perm, inv, gate, ys, c.T, c.d, c.k, y, st));
 }
 
+static moe_status stage_combine_ec(const moe_config& c, const float* y_perm, const int32_t* pos_of, const float* gate,
+                                   const float* ys, void* y, cudaStream_t st) {
+  return cuda_status(ec_combine(c.dtype, y_perm, pos_of, gate, ys, c.T, c.E, c.d, y, st));
+}
+
 static moe_status check_weights(const moe_config& c, const void* W1, const void* W2, const void* W3) {
   if (!W1 || !W2 || !W3) return MOE_ERR_INVALID_ARG;
   if (!aligned16(W1) || !aligned16(W2) || !aligned16(W3)) return MOE_ERR_INVALID_ARG;
@@ -234,6 +274,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   if ((idx_out && !aligned4(idx_out)) || (counts_out && !aligned4(counts_out))) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_weights(c, W1, W2, W3));
   MOE_TRY(check_shared(c, Ws1, Ws2, Ws3));
+  if (expert_choice(c) && (sb || idx_out || counts_out)) return MOE_ERR_UNSUPPORTED;
   const FwdLayout L = fwd_layout(c);
   if (!ws || !aligned16(ws)) return ws ? MOE_ERR_INVALID_ARG : MOE_ERR_WORKSPACE;
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -259,10 +300,17 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
     if (ev && ev[i]) return cuda_status(cudaEventRecord(ev[i], st));
     return MOE_OK;
   };
+  const bool ec = expert_choice(c);
   MOE_TRY(mark(0));
-  MOE_TRY(stage_route(c, x, W_g, lb, sb, idx, gate, logits, st));
-  MOE_TRY(mark(1));
-  MOE_TRY(stage_dispatch(c, idx, x, counts, offsets, perm, inv, x_perm, chunk_counts, chunk_base, st));
+  if (ec) {
+    MOE_TRY(stage_route_ec(c, x, W_g, lb, logits, offsets, perm, gate, inv, st));
+    MOE_TRY(mark(1));
+    MOE_CUDA(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, st));
+  } else {
+    MOE_TRY(stage_route(c, x, W_g, lb, sb, idx, gate, logits, st));
+    MOE_TRY(mark(1));
+    MOE_TRY(stage_dispatch(c, idx, x, counts, offsets, perm, inv, x_perm, chunk_counts, chunk_base, st));
+  }
   MOE_TRY(mark(2));
   MOE_TRY(stage_w12(c, x_perm, offsets, W1, W2, h, st));
   MOE_TRY(mark(3));
@@ -270,7 +318,11 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   MOE_TRY(mark(4));
   MOE_TRY(stage_shared(c, x, Ws1, Ws2, Ws3, hs, ys, st));
   MOE_TRY(mark(5));
-  MOE_TRY(stage_combine(c, y_perm, inv, gate, ys, y, st));
+  if (ec) {
+    MOE_TRY(stage_combine_ec(c, y_perm, inv, gate, ys, y, st));
+  } else {
+    MOE_TRY(stage_combine(c, y_perm, inv, gate, ys, y, st));
+  }
   MOE_TRY(mark(6));
   return MOE_OK;
 }
@@ -292,6 +344,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* W_g, cons
   g_launches = 0;
   MOE_TRY(check_config(cfg));
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;   // see moe_route_expert_choice
   if (c.T == 0) return MOE_OK;
   if (!x || !W_g || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned4(W_g) || !aligned4(topk_idx) || !aligned4(topk_gate)) return MOE_ERR_INVALID_ARG;
@@ -325,11 +378,7 @@ moe_status moe_load_stats(const moe_config* cfg, const void* x, const void* W_g,
   const cudaStream_t st = (cudaStream_t)stream;
   float* logits = static_cast<float*>(ws);
   float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + s.stats_logits);
-  if (c.dtype == MOE_BF16 && c.E % 8 == 0 && aligned16(W_g)) {
-    MOE_CUDA(tc_matmul_f32(x, c.T, c.d, W_g, 1, c.E, nullptr, 1, c.T, 0, logits, c.E, 0, error_word(), st));
-  } else {
-    MOE_CUDA(route_logits_simt(c.dtype, x, W_g, c.T, c.d, c.E, logits, st));
-  }
+  MOE_TRY(router_logits(c, x, W_g, logits, st));
   return cuda_status(load_stats(logits, logit_bias, counts, c.T, c.k, c.E, c.scoring, alpha, partial, f, P, summary,
                                 st));
 }
@@ -349,6 +398,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
   g_launches = 0;
   MOE_TRY(check_config(cfg));
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;   // see moe_route_expert_choice
   if (c.T == 0) return MOE_OK;
   if (!topk_idx || !x || !counts || !offsets || !perm_tok || !inv_pos || !x_perm) return MOE_ERR_INVALID_ARG;
   if (!aligned4(topk_idx) || !aligned4(counts) || !aligned4(offsets) || !aligned4(perm_tok) || !aligned4(inv_pos) ||
@@ -389,6 +439,7 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
   g_launches = 0;
   MOE_TRY(check_config(cfg));
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;   // see moe_route_expert_choice
   if (c.T == 0) return MOE_OK;
   if (!y_perm || !inv_pos || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned4(inv_pos) || !aligned4(topk_gate) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
@@ -405,6 +456,52 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
     MOE_TRY(stage_shared(c, x, Ws1, Ws2, Ws3, ws, ys, st));
   }
   return stage_combine(c, y_perm, inv_pos, topk_gate, ys, y, st);
+}
+
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const void* W_g, const float* logit_bias,
+                                   int32_t* offsets, int32_t* perm_tok, float* gate, int32_t* pos_of, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  g_launches = 0;
+  MOE_TRY(check_config(cfg));
+  const moe_config& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (!x || !W_g || !offsets || !perm_tok || !gate || !pos_of) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned4(W_g) || !aligned4(offsets) || !aligned4(perm_tok) || !aligned4(gate) ||
+      !aligned4(pos_of))
+    return MOE_ERR_INVALID_ARG;
+  if (logit_bias && !aligned4(logit_bias)) return MOE_ERR_INVALID_ARG;
+  const Sizes s = sizes(c);
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < s.logits) return MOE_ERR_WORKSPACE;
+  return stage_route_ec(c, x, W_g, logit_bias, static_cast<float*>(ws), offsets, perm_tok, gate, pos_of,
+                        (cudaStream_t)stream);
+}
+
+moe_status moe_combine_expert_choice(const moe_config* cfg, const float* y_perm, const float* gate,
+                                     const int32_t* pos_of, const void* x, const void* Ws1, const void* Ws2,
+                                     const void* Ws3, void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  g_launches = 0;
+  MOE_TRY(check_config(cfg));
+  const moe_config& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (!y_perm || !gate || !pos_of || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned4(gate) || !aligned4(pos_of) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  float* ys = nullptr;
+  if (c.n_shared > 0) {
+    if (!x || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_shared(c, Ws1, Ws2, Ws3));
+    const Sizes s = sizes(c);
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < s.hs + s.ys) return MOE_ERR_WORKSPACE;
+    ys = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + s.hs);
+    MOE_TRY(stage_shared(c, x, Ws1, Ws2, Ws3, ws, ys, st));
+  }
+  return stage_combine_ec(c, y_perm, pos_of, gate, ys, y, st);
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const float* logit_bias,
@@ -515,6 +612,7 @@ extern "C" moe_status moe_dispatch_static(const moe_config* cfg, const int32_t* 
   g_launches = 0;
   MOE_TRY(check_config(cfg));
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_UNSUPPORTED;   // see moe_route_expert_choice
   if (c.T == 0) return MOE_OK;
   if (!topk_idx || !x || !counts || !offsets || !perm_tok || !inv_pos || !x_perm) return MOE_ERR_INVALID_ARG;
   if (!aligned4(topk_idx) || !aligned4(counts) || !aligned4(offsets) || !aligned4(perm_tok) || !aligned4(inv_pos) ||

@@ -21,9 +21,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
 MOE_F32, MOE_BF16 = 0, 1
-MOE_SOFTMAX_TOPK_RENORM, MOE_SIGMOID_TOPK_NORM, MOE_SOFTMAX_TOPK_PLAIN = 0, 1, 2
+MOE_SOFTMAX_TOPK_RENORM, MOE_SIGMOID_TOPK_NORM, MOE_SOFTMAX_TOPK_PLAIN, MOE_EXPERT_CHOICE = 0, 1, 2, 3
 SCORING = {"softmax": MOE_SOFTMAX_TOPK_RENORM, "sigmoid": MOE_SIGMOID_TOPK_NORM,
-           "softmax_norenorm": MOE_SOFTMAX_TOPK_PLAIN}
+           "softmax_norenorm": MOE_SOFTMAX_TOPK_PLAIN, "expert_choice": MOE_EXPERT_CHOICE}
 MOE_NUM_STAGES = 6
 STAGE_NAMES = ("route", "dispatch", "experts_w12", "experts_w3", "shared", "combine")
 
@@ -67,13 +67,15 @@ _last_launch_count = _sig("moe_last_launch_count", [], ctypes.c_int32)
 _status_string = _sig("moe_status_string", [_I], ctypes.c_char_p)
 _dispatch_static = _sig("moe_dispatch_static", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P])
 _update_sel_bias = _sig("moe_update_sel_bias", [_CFG, _P, ctypes.c_float, _P, _P])
+_route_ec = _sig("moe_route_expert_choice", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P])
+_combine_ec = _sig("moe_combine_expert_choice", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P])
 _load_stats = _sig("moe_load_stats", [_CFG, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _SZ, _P])
 DISPATCH_STATIC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts", "moe_combine",
            "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_get_device_error",
            "moe_last_launch_count", "moe_status_string", "moe_dispatch_static", "moe_update_sel_bias",
-           "moe_load_stats")
+           "moe_load_stats", "moe_route_expert_choice", "moe_combine_expert_choice")
 
 
 def status_string(status: int) -> str:
@@ -136,6 +138,21 @@ def dispatch_static(cfg, topk_idx, x, counts, offsets, perm_tok, inv_pos, x_perm
     scratch is a fixed 1 MiB array inside the library (size limit and sharing rules in moe.h)."""
     _check(_dispatch_static(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
                             _ptr(inv_pos), _ptr(x_perm), _stream(stream)), "moe_dispatch_static")
+
+
+def route_expert_choice(cfg, x, W_g, offsets, perm_tok, gate, pos_of, logit_bias=None, ws=None, ws_bytes=None,
+                        stream=None):
+    """Expert choice: every expert's m tokens (offsets = e*m, perm_tok, gate by position, pos_of [T][E])."""
+    nb = ws.numel() * ws.element_size() if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    _check(_route_ec(ctypes.byref(cfg), _ptr(x), _ptr(W_g), _ptr(logit_bias), _ptr(offsets), _ptr(perm_tok),
+                     _ptr(gate), _ptr(pos_of), _ptr(ws), nb, _stream(stream)), "moe_route_expert_choice")
+
+
+def combine_expert_choice(cfg, y_perm, gate, pos_of, y, x=None, Ws1=None, Ws2=None, Ws3=None, ws=None, ws_bytes=None,
+                          stream=None):
+    nb = ws.numel() * ws.element_size() if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    _check(_combine_ec(ctypes.byref(cfg), _ptr(y_perm), _ptr(gate), _ptr(pos_of), _ptr(x), _ptr(Ws1), _ptr(Ws2),
+                       _ptr(Ws3), _ptr(y), _ptr(ws), nb, _stream(stream)), "moe_combine_expert_choice")
 
 
 def load_stats(cfg, x, W_g, counts, alpha, f, P, summary, logit_bias=None, ws=None, ws_bytes=None, stream=None):

@@ -43,6 +43,36 @@ def gapped_attempts(shape: wl.MoEShape, seed: int = 0, min_gap: float = 1e-3,
     raise RuntimeError("could not separate the router logits of %d tokens" % rows.size)
 
 
+def expert_choice_gapped_attempts(shape: wl.MoEShape, m: int, seed: int = 0, min_rel_gap: float = 1e-4,
+                                  max_rounds: int = 200) -> np.ndarray:
+    """Per-token attempt counters for expert choice: for every expert, the m-th and (m+1)-th
+    largest float32 scores s[:, e] differ by at least min_rel_gap of the m-th, so every
+    expert's set of m tokens is unique (the GPU's scores differ from the oracle's by a few
+    ulps).  The two tokens at an expert's boundary are redrawn until that holds."""
+    T, E = shape.T, shape.E
+    Wg = wl.to_f64(wl.gen_router(shape, seed), shape.dtype)
+    lb = wl.gen_logit_bias(shape, seed)
+    attempts = np.zeros(T, dtype=np.int64)
+    x = wl.gen_x(shape, seed, attempts)
+    if m >= T:
+        return attempts
+    for _ in range(max_rounds):
+        l = orc.router_logits(wl.to_f64(x, shape.dtype), Wg, lb)
+        key = orc.scores(l, "softmax").astype(np.float32).astype(np.float64)
+        bad = set()
+        for e in range(E):
+            order = np.argsort(-key[:, e], kind="stable")
+            a, b = key[order[m - 1], e], key[order[m], e]
+            if a - b < min_rel_gap * a:
+                bad.update((int(order[m - 1]), int(order[m])))
+        if not bad:
+            return attempts
+        rows = np.array(sorted(bad))
+        attempts[rows] += 1
+        x[rows] = wl.gen_x(shape, seed, attempts, rows=rows)
+    raise RuntimeError("could not separate the expert-choice boundaries")
+
+
 class Case:
     """Host inputs of one workload plus float64 views for the oracle.
 
@@ -54,7 +84,14 @@ class Case:
         self.shape = shape
         self.seed = seed
         self.sel_bias = sel_bias
-        self.attempts = gapped_attempts(shape, seed, sel_bias=sel_bias) if gap else np.zeros(shape.T, np.int64)
+        self.ec_m = (orc.expert_choice_slots(shape.T, shape.k, shape.E, shape.capacity_factor)
+                     if shape.scoring == "expert_choice" else None)
+        if not gap:
+            self.attempts = np.zeros(shape.T, np.int64)
+        elif self.ec_m is not None:
+            self.attempts = expert_choice_gapped_attempts(shape, self.ec_m, seed)
+        else:
+            self.attempts = gapped_attempts(shape, seed, sel_bias=sel_bias)
         self.x = wl.gen_x(shape, seed, self.attempts)
         self.W_g = wl.gen_router(shape, seed)
         self.logit_bias = wl.gen_logit_bias(shape, seed)
@@ -83,5 +120,8 @@ class Case:
 
     def forward(self):
         s = self.shape
+        if self.ec_m is not None:
+            return orc.expert_choice_forward(self.f64(self.x), self.f64(self.W_g), self.get_w, s.E, self.ec_m,
+                                             self.logit_bias, s.n_shared)
         return orc.forward(self.f64(self.x), self.f64(self.W_g), self.get_w, s.E, s.k, s.scoring,
                            self.logit_bias, self.sel_bias, s.n_shared, s.capacity_factor)

@@ -18,7 +18,7 @@ Sources (page title, section):
   [FM]  "Mixture-of-Experts Internals: A Systems Engineer's Field Manual": section 2.1
         (softmax over all E, top-k, renormalise over the chosen k), section 3.2 (Switch
         auxiliary loss), section 3.3 (bias used only for selection), section 4.2 (dispatch
-        volume).
+        volume), section 5.1 (expert choice: each expert takes its top-m tokens).
   [RA]  "Mixture-of-Experts, from the router to the all-to-all": "The router" (sigmoid
         scores normalised over the chosen k; Switch's top-1 y = p_i(x) E_i(x) without
         renormalisation), "Experts, fine-grained and shared" (P_e =
@@ -330,6 +330,88 @@ def forward_bruteforce(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: in
                     taken += 1
                     f = swiglu_expert(x64[t:t + 1], get_w("W1", e), get_w("W2", e), get_w("W3", e))[0]
                     y[t] += r["gate"][t, j] * f
+    ys = shared_experts(x64, get_w, n_shared)
+    return y if ys is None else y + ys
+
+
+# --------------------------------------------------------------------------------------
+# Expert-choice routing
+# --------------------------------------------------------------------------------------
+
+
+def expert_choice_slots(T: int, k: int, E: int, factor: float) -> int:
+    """Tokens each expert takes under expert choice: m = ceil(T k c / E) with c the capacity
+    factor (1 when none is given), at most T.  [FM] section 5.1: each expert chooses its
+    top-m tokens, exactly m per expert; the capacity formula is that of [MM] section 3.2."""
+    c = factor if factor > 0 else 1.0
+    return min(T, capacity_slots(T, k, E, c))
+
+
+def expert_choice_route(x64: np.ndarray, Wg64: np.ndarray, E: int, m: int,
+                        logit_bias: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Expert choice ([FM] section 5.1; [RA] "Load balancing": each expert takes its top
+    tokens, so load is balanced by construction).  The token-to-expert scores are the softmax
+    over the experts of each token's router logits; expert e takes the m tokens with the
+    largest s[t, e] (decided on float32 values; equal values go to the lower token id) and
+    weights its output for token t by s[t, e].  A token may be taken by any number of
+    experts, including none.
+
+    Returns offsets [E+1] (= e m), perm_tok [E m] (each expert's tokens in ascending token
+    order), gate [E m] float64, pos_of [T, E] int32 (the position of (t, e), or -1),
+    logits, scores."""
+    l = router_logits(x64, Wg64, logit_bias)
+    s = scores(l, "softmax")
+    key = s.astype(np.float32)
+    T = l.shape[0]
+    perm, gate = [], []
+    pos_of = np.full((T, E), -1, dtype=np.int32)
+    for e in range(E):
+        order = np.argsort(-key[:, e], kind="stable")
+        toks = np.sort(order[:m])
+        for r, t in enumerate(toks):
+            pos_of[t, e] = e * m + r
+        perm.append(toks)
+        gate.append(s[toks, e])
+    return {"offsets": (np.arange(E + 1) * m).astype(np.int32),
+            "perm_tok": np.concatenate(perm).astype(np.int32) if E else np.zeros(0, np.int32),
+            "gate": np.concatenate(gate) if E else np.zeros(0), "pos_of": pos_of, "logits": l, "scores": s}
+
+
+def expert_choice_forward(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, m: int,
+                          logit_bias=None, n_shared: int = 0) -> Dict[str, np.ndarray]:
+    """The layer under expert choice, grouped: each expert runs once on its m tokens, and
+    y[t] = sum over the experts that took t of s[t, e] f_e(x_t) (+ shared experts), summed in
+    expert order."""
+    r = expert_choice_route(x64, Wg64, E, m, logit_bias)
+    y_perm = experts_grouped(x64[r["perm_tok"]], r["offsets"], get_w)
+    T = x64.shape[0]
+    y = np.zeros((T, x64.shape[1]), np.float64)
+    for e in range(E):
+        p = r["pos_of"][:, e]
+        took = p >= 0
+        y[took] += r["gate"][p[took]][:, None] * y_perm[p[took]]
+    ys = shared_experts(x64, get_w, n_shared)
+    if ys is not None:
+        y = y + ys
+    out = dict(r)
+    out.update({"y_perm": y_perm, "y": y})
+    return out
+
+
+def expert_choice_bruteforce(x64: np.ndarray, Wg64: np.ndarray, get_w: WeightFn, E: int, m: int,
+                             logit_bias=None, n_shared: int = 0) -> np.ndarray:
+    """Expert choice evaluated naively: for every expert, rank all tokens by their score for
+    it with a full sort, keep the first m, run the expert on each kept token alone and add
+    s[t, e] times its output to that token."""
+    l = router_logits(x64, Wg64, logit_bias)
+    s = scores(l, "softmax")
+    T = x64.shape[0]
+    y = np.zeros((T, x64.shape[1]), np.float64)
+    for e in range(E):
+        ranked = sorted(range(T), key=lambda t: (-float(np.float32(s[t, e])), t))
+        for t in ranked[:m]:
+            f = swiglu_expert(x64[t:t + 1], get_w("W1", e), get_w("W2", e), get_w("W3", e))[0]
+            y[t] += s[t, e] * f
     ys = shared_experts(x64, get_w, n_shared)
     return y if ys is None else y + ys
 

@@ -359,6 +359,37 @@ def check_capacity_grouped_equals_bruteforce():
     assert np.array_equal(g["y"], n["y"]) and np.array_equal(g["inv_pos"], n["inv_pos"])
 
 
+def check_expert_choice():
+    # Balanced by construction ([FM] 5.1): every expert takes exactly m tokens; the grouped
+    # evaluation equals the naive per-expert full sort; gates are the token's softmax score.
+    x, Wg, W = _rand_layer(27, T=20, d=6, d_ff=5, E=4)
+    m = orc.expert_choice_slots(20, 2, 4, 0.0)
+    assert m == 10
+    g = orc.expert_choice_forward(x, Wg, _arrays_fn(W), 4, m)
+    assert np.array_equal(np.diff(g["offsets"]), [m] * 4)
+    assert ((g["pos_of"] >= 0).sum(axis=0) == m).all()
+    b = orc.expert_choice_bruteforce(x, Wg, _arrays_fn(W), 4, m)
+    assert np.allclose(g["y"], b, rtol=1e-12, atol=1e-12)
+    s = orc.scores(orc.router_logits(x, Wg), "softmax")
+    for e in range(4):
+        toks = g["perm_tok"][e * m:(e + 1) * m]
+        assert list(toks) == sorted(toks)
+        assert np.allclose(g["gate"][e * m:(e + 1) * m], s[toks, e], rtol=1e-15)
+        # the chosen tokens are the m largest of the column
+        assert s[toks, e].min() >= np.sort(s[:, e])[-m]
+    # every expert takes every token (m = T): the softmax-weighted dense ensemble, which is
+    # token choice with k = E
+    full = orc.expert_choice_forward(x, Wg, _arrays_fn(W), 4, 20)
+    dense = orc.forward(x, Wg, _arrays_fn(W), 4, 4, "softmax")
+    assert np.allclose(full["y"], dense["y"], rtol=1e-12, atol=1e-12)
+    # one expert that takes every token: gate 1, a dense SwiGLU FFN
+    x1, Wg1, W1 = _rand_layer(28, T=5, d=4, d_ff=3, E=1)
+    one = orc.expert_choice_forward(x1, Wg1, _arrays_fn(W1), 1, 5)
+    assert np.allclose(one["y"], dense_swiglu_loops(x1, W1["W1"][0], W1["W2"][0], W1["W3"][0]), rtol=1e-12)
+    # slots: ceil(T k c / E), at most T
+    assert orc.expert_choice_slots(100, 2, 8, 1.25) == 32 and orc.expert_choice_slots(10, 4, 2, 2.0) == 10
+
+
 def check_printed_values():
     G = json.load(open(GOLDEN))
     for c in G["combinations"]:
@@ -403,7 +434,8 @@ CHECKS = [check_router_logits_closed_form, check_scores_closed_forms, check_topk
           check_E1_k1_is_dense_swiglu, check_grouped_equals_bruteforce, check_shared_only,
           check_selection_bias, check_selection_bias_sigmoid_uses_scores, check_sel_bias_update_closed_form,
           check_bias_controller_balances, check_switch_top1_no_renorm, check_load_stats,
-          check_capacity_dropping, check_capacity_grouped_equals_bruteforce, check_printed_values]
+          check_capacity_dropping, check_capacity_grouped_equals_bruteforce, check_expert_choice,
+          check_printed_values]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -473,6 +505,11 @@ def _drop_earliest(idx, E, slots=None):                       # an expert keeps 
     return {"counts": rev["counts"], "offsets": rev["offsets"], "perm_tok": rev["perm_tok"], "inv_pos": inv}
 
 
+def _ec_lowest(x64, Wg64, E, m, logit_bias=None):               # experts take their m LOWEST scores
+    r = orc.__dict__["_orig_expert_choice_route"](-np.asarray(x64), Wg64, E, m, logit_bias)
+    return r
+
+
 PLANTS = [
     ("swiglu_expert", _swapped_swiglu, [check_swiglu_scalar_closed_form, check_swiglu_vs_loops]),
     ("gates_from_scores", _no_renorm, [check_gate_invariants, check_gates_two_formulations]),
@@ -485,6 +522,7 @@ PLANTS = [
     ("selection_keys", _bias_on_logits, [check_selection_bias_sigmoid_uses_scores]),
     ("aux_loss", _aux_without_E, [check_load_stats]),
     ("dispatch", _drop_earliest, [check_capacity_dropping, check_capacity_grouped_equals_bruteforce]),
+    ("expert_choice_route", _ec_lowest, [check_expert_choice]),
 ]
 
 
