@@ -278,6 +278,15 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
    MOE_ERR_CUDA when the wait itself failed. */
 moe_status moe_get_device_error(moe_stream_t stream, uint32_t* word);
 
+/* Testing aid for the failure detection of the pipelined GEMM kernels (the pages have no
+   counterpart): the next grouped tensor-core GEMM that this process launches gets a TMA
+   producer that issues no copies, and every pipeline wait of that launch gives up after
+   wait_limit_ns (1 .. 2e9) instead of 2 s.  Its waits then run out one after another, the
+   kernel sets the device error word (MMA and epilogue wait bits), frees its tensor memory and
+   returns; nothing faults and the CUDA context stays usable.  The results of that launch are
+   garbage.  Later launches are unaffected. */
+moe_status moe_test_pipeline_fault(uint64_t wait_limit_ns);
+
 /* Number of kernels the last call on this host thread launched. */
 int32_t moe_last_launch_count(void);
 

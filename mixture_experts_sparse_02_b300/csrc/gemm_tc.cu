@@ -23,6 +23,7 @@
 // allocation; warp 3 builds the group table.  Every wait is bounded (kWaitLimitNs) and on a
 // timeout sets the device error word and unwinds.
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <stdlib.h>
 #include <string.h>
 
@@ -227,12 +228,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int s = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
-      bool ok = true;
+      bool ok = !a.starve;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode_tile(c, G, t);
         const int z = a.offsets ? tl.g : a.b_z;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort)) {
+          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort, a.wait_limit_ns)) {
             flag_error(a.err, ERR_WAIT_PRODUCER);
             c.abort = 1;
             ok = false;
@@ -263,7 +264,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // Let the copies already issued land before the CTA's shared memory is released.
         volatile int never = 0;
         for (int i = 0; i < STAGES; ++i)
-          if (armed & (1u << i)) mbar_wait(&c.full[i], (armed_parity >> i) & 1u, &never);
+          if (armed & (1u << i)) mbar_wait(&c.full[i], (armed_parity >> i) & 1u, &never, a.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -276,11 +277,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort)) { ok = false; break; }
+        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&c.full[s], phase, &c.abort)) { ok = false; break; }
+          if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
           const uint32_t sb = sa + A_TILE;
@@ -305,7 +306,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // Wait for the MMAs already issued before TMEM is released.
         umma_commit(&c.drain);
         volatile int never = 0;
-        mbar_wait(&c.drain, 0, &never);
+        mbar_wait(&c.drain, 0, &never, a.wait_limit_ns);
       }
     }
   } else if (warp >= 4) {
@@ -317,7 +318,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       // Warp-uniform decision: the TMEM loads below are .sync.aligned.
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort, a.wait_limit_ns));
       if (!got) {
         if (lane == 0) flag_error(a.err, ERR_WAIT_EPILOGUE);
         c.abort = 1;
@@ -437,13 +438,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       // ---------------------------------------------------------------- TMA producer (both CTAs)
       int s = 0;
       uint32_t phase = 0;
-      for (int t = cid; t < total; t += nclusters) {
+      for (int t = a.starve ? total : cid; t < total; t += nclusters) {
         const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
         const int z = a.offsets ? tl.g : a.b_z;
         const int arow = tl.row0 + (int)rank * pair::BM;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort)) {
+          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort, a.wait_limit_ns)) {
             flag_error(a.err, ERR_WAIT_PRODUCER);
             c.abort = 1;
             ok = false;
@@ -480,11 +481,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       for (int t = cid; t < total && ok; t += nclusters, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort)) { ok = false; break; }
+        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&c.full[s], phase, &c.abort)) { ok = false; break; }
+          if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
           const uint32_t sb = sa + pair::A_TILE;
@@ -507,7 +508,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         c.abort = 1;
         umma_commit_pair(&c.drain, 0x1);
         volatile int never = 0;
-        mbar_wait(&c.drain, 0, &never);
+        mbar_wait(&c.drain, 0, &never, a.wait_limit_ns);
       }
     }
   } else if (warp >= 4) {
@@ -520,7 +521,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort, a.wait_limit_ns));
       if (!got) {
         if (lane == 0) flag_error(a.err, ERR_WAIT_EPILOGUE);
         c.abort = 1;
@@ -650,6 +651,19 @@ static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, co
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Test hook: one starved launch with a short wait limit (moe_test_pipeline_fault).
+static std::atomic<unsigned long long> g_fault_limit_ns{0};
+
+static void apply_test_hook(GemmArgs& a) {
+  a.wait_limit_ns = kWaitLimitNs;
+  a.starve = 0;
+  const unsigned long long lim = g_fault_limit_ns.exchange(0);
+  if (lim) {
+    a.wait_limit_ns = lim;
+    a.starve = 1;
+  }
+}
+
 // Kernel choice: "pair" tiles are 256 rows, so they pay off when groups are large; the
 // single-CTA kernel (128-row tiles) wastes fewer rows on small or ragged groups.  The
 // environment variable MOE_GEMM_KERNEL=single|pair overrides the choice (used by the tests to
@@ -663,6 +677,10 @@ static bool use_pair(long long rows, int groups) {
 
 }  // namespace tc
 
+void arm_pipeline_fault(unsigned long long wait_limit_ns) {
+  tc::g_fault_limit_ns.store(wait_limit_ns ? wait_limit_ns : 1);
+}
+
 // h[rows, N] (bf16) = (A W1) * SiLU(A W2), grouped.  A is [rows_cap, K] bf16; W1, W2 are
 // [Z][K][N] bf16.  N must be a multiple of 8, K a multiple of 8.
 cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, const void* W2, int Z, int N,
@@ -674,6 +692,7 @@ cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, 
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
   a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);
   a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
+  tc::apply_test_hook(a);
   if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
     return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
   return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
@@ -689,6 +708,7 @@ cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* 
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
   a.n_tiles = (N + tc::BN - 1) / tc::BN;
   a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
+  tc::apply_test_hook(a);
   if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
     return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
   return tc::launch<EPI_F32>(ma, mb, mb, a, st);

@@ -25,7 +25,13 @@ struct GemmArgs {
   int accumulate;      // EPI_F32: out += result
   int rows_cap;        // rows of A and of out; offsets beyond it are clamped and flagged
   uint32_t* err;       // device error word
+  unsigned long long wait_limit_ns;  // bound of every pipeline wait
+  int starve;          // test hook: the TMA producer issues no copies (the waits run out)
 };
+
+// Test hook (moe_test_pipeline_fault): arm a starved pipeline with a short wait limit for the
+// next grouped tensor-core GEMM launch of this process.
+void arm_pipeline_fault(unsigned long long wait_limit_ns);
 
 // ---- tensor-core (bf16) path
 cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, const void* W2, int Z, int N,

@@ -562,6 +562,12 @@ moe_status moe_get_device_error(moe_stream_t stream, uint32_t* word) {
 
 int32_t moe_last_launch_count(void) { return g_launches; }
 
+moe_status moe_test_pipeline_fault(uint64_t wait_limit_ns) {
+  if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return MOE_ERR_INVALID_ARG;
+  arm_pipeline_fault((unsigned long long)wait_limit_ns);
+  return MOE_OK;
+}
+
 const char* moe_status_string(moe_status status) {
   switch (status) {
     case MOE_OK: return "ok";

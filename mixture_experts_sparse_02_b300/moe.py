@@ -69,13 +69,14 @@ _dispatch_static = _sig("moe_dispatch_static", [_CFG, _P, _P, _P, _P, _P, _P, _P
 _update_sel_bias = _sig("moe_update_sel_bias", [_CFG, _P, ctypes.c_float, _P, _P])
 _route_ec = _sig("moe_route_expert_choice", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P])
 _combine_ec = _sig("moe_combine_expert_choice", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P])
+_test_pipeline_fault = _sig("moe_test_pipeline_fault", [ctypes.c_uint64])
 _load_stats = _sig("moe_load_stats", [_CFG, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _SZ, _P])
 DISPATCH_STATIC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts", "moe_combine",
            "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_get_device_error",
            "moe_last_launch_count", "moe_status_string", "moe_dispatch_static", "moe_update_sel_bias",
-           "moe_load_stats", "moe_route_expert_choice", "moe_combine_expert_choice")
+           "moe_load_stats", "moe_route_expert_choice", "moe_combine_expert_choice", "moe_test_pipeline_fault")
 
 
 def status_string(status: int) -> str:
@@ -218,6 +219,12 @@ def get_device_error(stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE):
         raise MoEError(st, "moe_get_device_error")
     return int(w.value)
+
+
+def test_pipeline_fault(wait_limit_ns: int):
+    """Testing aid: starve the next grouped tensor-core GEMM launch (its waits run out after
+    wait_limit_ns and it reports through the device error word)."""
+    _check(_test_pipeline_fault(int(wait_limit_ns)), "moe_test_pipeline_fault")
 
 
 def last_launch_count() -> int:
