@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restri
                                                           const float* __restrict__ gate,
                                                           const float4* __restrict__ ys, int T, int d4, int k,
                                                           long long rows_perm, void* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_pos[32];
   __shared__ float s_g[32];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -58,6 +60,8 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
                                                              const float* __restrict__ gate,
                                                              const float* __restrict__ ys, int T, int d, int k,
                                                              long long rows_perm, void* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
       float acc = 0.f;
@@ -85,16 +89,17 @@ cudaError_t combine(int dtype, const float* y_perm, const int32_t* inv_pos, cons
                    ((uintptr_t)y % (dtype == 1 ? 8 : 16) == 0);
   if (vec) {
     if (dtype == 1)
-      combine_vec_kernel<true><<<blocks, 256, 0, st>>>((const float4*)y_perm, inv_pos, gate, (const float4*)ys, T,
-                                                       d / 4, k, rows_perm, y);
+      MOE_RETURN_ON_ERROR(launch_k(combine_vec_kernel<true>, blocks, 256, 0, st, (const float4*)y_perm, inv_pos, gate,
+                         (const float4*)ys, T, d / 4, k, rows_perm, y));
     else
-      combine_vec_kernel<false><<<blocks, 256, 0, st>>>((const float4*)y_perm, inv_pos, gate, (const float4*)ys, T,
-                                                        d / 4, k, rows_perm, y);
+      MOE_RETURN_ON_ERROR(launch_k(combine_vec_kernel<false>, blocks, 256, 0, st, (const float4*)y_perm, inv_pos, gate,
+                         (const float4*)ys, T, d / 4, k, rows_perm, y));
   } else {
     if (dtype == 1)
-      combine_scalar_kernel<true><<<blocks, 256, 0, st>>>(y_perm, inv_pos, gate, ys, T, d, k, rows_perm, y);
+      MOE_RETURN_ON_ERROR(launch_k(combine_scalar_kernel<true>, blocks, 256, 0, st, y_perm, inv_pos, gate, ys, T, d, k, rows_perm, y));
     else
-      combine_scalar_kernel<false><<<blocks, 256, 0, st>>>(y_perm, inv_pos, gate, ys, T, d, k, rows_perm, y);
+      MOE_RETURN_ON_ERROR(launch_k(combine_scalar_kernel<false>, blocks, 256, 0, st, y_perm, inv_pos, gate, ys, T, d, k, rows_perm,
+                         y));
   }
   ++g_launches;
   return cudaGetLastError();

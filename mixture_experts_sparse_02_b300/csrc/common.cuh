@@ -53,6 +53,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------------------- dependent launch
+// Every kernel of the library is launched with programmatic stream serialization, so that it
+// may be scheduled while the previous kernel in the stream is still finishing.  pdl_wait()
+// blocks until the previous kernel has completed and its writes are visible: each kernel
+// calls it before it reads or writes any global memory that an earlier kernel of the stream
+// writes or reads.  pdl_trigger() lets the next kernel launch early (its own pdl_wait still
+// waits for this kernel to complete).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -293,6 +303,30 @@ template <int M, int N>
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_kmaj_a_mnmaj_b() {
   return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+
+// Returns from the enclosing function if `expr` (a cudaError_t) is not cudaSuccess.
+#define MOE_RETURN_ON_ERROR(expr)             \
+  do {                                        \
+    const cudaError_t e__ = (expr);           \
+    if (e__ != cudaSuccess) return e__;       \
+  } while (0)
+
+// Host: launch `kernel` on `st` with programmatic stream serialization (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace moe

@@ -33,6 +33,8 @@ constexpr unsigned FULL = 0xffffffffu;
 __global__ void __launch_bounds__(WARPS * 32) hist_kernel(const int32_t* __restrict__ idx, long long N, int E,
                                                           int n_chunks, int32_t* __restrict__ chunk_counts,
                                                           uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * WARPS + warp;
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(WARPS * 32) hist_kernel(const int32_t* __restr
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts, int n_chunks, int E,
                                                     int S, int cap, int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int part[1024];   // [S][E] segment sums, then exclusive segment bases
   __shared__ int tot[1024];    // per-expert totals, then offsets
   __shared__ int wsum[32];
@@ -131,6 +135,8 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
                                                              const int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ perm_tok,
                                                              int32_t* __restrict__ inv_pos) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * WARPS + warp;
@@ -171,6 +177,8 @@ template <typename V>
 __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, const int32_t* __restrict__ perm_tok,
                                                      long long rows, const int32_t* __restrict__ rows_dev,
                                                      int vec_per_row, long long T, V* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   if (rows_dev) {   // rows actually kept (offsets[E]); never more than the buffer holds
@@ -197,16 +205,13 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int c
   const int n_chunks = dispatch_num_chunks(N);
   const unsigned blocks = (unsigned)((n_chunks + WARPS - 1) / WARPS);
   const size_t shm = (size_t)WARPS * E * sizeof(int);
-  hist_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, E, n_chunks, chunk_counts, err);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  MOE_RETURN_ON_ERROR(launch_k(hist_kernel, blocks, WARPS * 32, shm, st, topk_idx, N, E, n_chunks, chunk_counts, err));
   int S = 1;
   while (S * 2 * E <= 1024 && S * 2 <= n_chunks) S *= 2;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, n_chunks, E, S, cap, chunk_base, counts, offsets);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  permute_kernel<<<blocks, WARPS * 32, shm, st>>>(topk_idx, N, k, E, n_chunks, cap, chunk_base, offsets, perm_tok,
-                                                  inv_pos);
+  MOE_RETURN_ON_ERROR(launch_k(scan_kernel, 1, 1024, 0, st, chunk_counts, n_chunks, E, S, cap, chunk_base, counts,
+                               offsets));
+  MOE_RETURN_ON_ERROR(launch_k(permute_kernel, blocks, WARPS * 32, shm, st, topk_idx, N, k, E, n_chunks, cap,
+                               chunk_base, offsets, perm_tok, inv_pos));
   g_launches += 3;
   if (launches) *launches += 3;
   return cudaGetLastError();
@@ -219,14 +224,14 @@ cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, lon
   long long want = (rows * 32 + threads - 1) / threads;
   const unsigned blocks = (unsigned)(want < 148LL * 16 ? want : 148LL * 16);
   if (row_bytes % 16 == 0 && ((uintptr_t)x % 16 == 0) && ((uintptr_t)x_perm % 16 == 0)) {
-    gather_kernel<uint4><<<blocks, threads, 0, st>>>((const uint4*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 16), T,
-                                                     (uint4*)x_perm);
+    MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint4>, blocks, threads, 0, st, (const uint4*)x, perm_tok, rows, rows_dev,
+                                 (int)(row_bytes / 16), T, (uint4*)x_perm));
   } else if (row_bytes % 4 == 0) {
-    gather_kernel<uint32_t><<<blocks, threads, 0, st>>>((const uint32_t*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 4), T,
-                                                        (uint32_t*)x_perm);
+    MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint32_t>, blocks, threads, 0, st, (const uint32_t*)x, perm_tok, rows,
+                                 rows_dev, (int)(row_bytes / 4), T, (uint32_t*)x_perm));
   } else {
-    gather_kernel<uint16_t><<<blocks, threads, 0, st>>>((const uint16_t*)x, perm_tok, rows, rows_dev, (int)(row_bytes / 2), T,
-                                                        (uint16_t*)x_perm);
+    MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint16_t>, blocks, threads, 0, st, (const uint16_t*)x, perm_tok, rows,
+                                 rows_dev, (int)(row_bytes / 2), T, (uint16_t*)x_perm));
   }
   ++g_launches;
   return cudaGetLastError();

@@ -30,6 +30,8 @@ constexpr unsigned FULL = 0xffffffffu;
 template <int EPL>
 __global__ void __launch_bounds__(256) ec_scores_kernel(float* __restrict__ s, const float* __restrict__ lb, int T,
                                                         int E) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -93,6 +95,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total
 __global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict__ s, int T, int E, int m,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm_tok,
                                                          float* __restrict__ gate, int32_t* __restrict__ pos_of) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t keys[];   // [T]
   __shared__ int hist[256];
   __shared__ int wsum[33];
@@ -166,6 +170,8 @@ __global__ void __launch_bounds__(256) ec_combine_kernel(const float4* __restric
                                                          const int32_t* __restrict__ pos_of,
                                                          const float* __restrict__ gate, const float4* __restrict__ ys,
                                                          int T, int E, int d4, void* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sh[];   // [E] positions, then [E] gates, of the experts that took t
   int* s_pos = sh;
   float* s_g = reinterpret_cast<float*>(sh + E);
@@ -229,7 +235,7 @@ size_t ec_select_smem(int T) { return (size_t)T * sizeof(uint32_t); }
 cudaError_t ec_route(float* scores, const float* logit_bias, int T, int E, int m, int32_t* offsets,
                      int32_t* perm_tok, float* gate, int32_t* pos_of, cudaStream_t st) {
   const unsigned blocks = (unsigned)(((long long)T * 32 + 255) / 256);
-#define MOE_EC_SCORES(EPL) ec_scores_kernel<EPL><<<blocks, 256, 0, st>>>(scores, logit_bias, T, E)
+#define MOE_EC_SCORES(EPL) MOE_RETURN_ON_ERROR(launch_k(ec_scores_kernel<EPL>, blocks, 256, 0, st, scores, logit_bias, T, E))
   if (E <= 32) MOE_EC_SCORES(1);
   else if (E <= 64) MOE_EC_SCORES(2);
   else if (E <= 128) MOE_EC_SCORES(4);
@@ -245,7 +251,8 @@ cudaError_t ec_route(float* scores, const float* logit_bias, int T, int E, int m
     e = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  ec_select_kernel<<<E, 1024, smem, st>>>(scores, T, E, m, offsets, perm_tok, gate, pos_of);
+  MOE_RETURN_ON_ERROR(launch_k(ec_select_kernel, E, 1024, smem, st, (const float*)scores, T, E, m, offsets, perm_tok,
+                               gate, pos_of));
   ++g_launches;
   return cudaGetLastError();
 }
@@ -255,11 +262,11 @@ cudaError_t ec_combine(int dtype, const float* y_perm, const int32_t* pos_of, co
   const unsigned blocks = (unsigned)(T < 148 * 16 ? T : 148 * 16);
   const size_t smem = (size_t)E * 8;
   if (dtype == 1)
-    ec_combine_kernel<true><<<blocks, 256, smem, st>>>((const float4*)y_perm, pos_of, gate, (const float4*)ys, T, E,
-                                                       d / 4, y);
+    MOE_RETURN_ON_ERROR(launch_k(ec_combine_kernel<true>, blocks, 256, smem, st, (const float4*)y_perm, pos_of, gate,
+                                 (const float4*)ys, T, E, d / 4, y));
   else
-    ec_combine_kernel<false><<<blocks, 256, smem, st>>>((const float4*)y_perm, pos_of, gate, (const float4*)ys, T, E,
-                                                        d / 4, y);
+    MOE_RETURN_ON_ERROR(launch_k(ec_combine_kernel<false>, blocks, 256, smem, st, (const float4*)y_perm, pos_of, gate,
+                                 (const float4*)ys, T, E, d / 4, y));
   ++g_launches;
   return cudaGetLastError();
 }

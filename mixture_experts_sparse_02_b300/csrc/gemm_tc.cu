@@ -213,6 +213,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tmem_alloc(&c.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();      // offsets, A and the outputs belong to earlier kernels of the stream
+  pdl_trigger();
   if (warp == 3) build_group_table<BM>(c, a, G, lane);
   tc_fence_before_sync();
   __syncthreads();
@@ -424,6 +426,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     prefetch_tensormap(&tmB1);
   }
   if (warp == 2) tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+  pdl_wait();      // offsets, A and the outputs belong to earlier kernels of the stream
+  pdl_trigger();
   if (warp == 3) build_group_table<pair::PAIR_M>(c, a, G, lane);
   tc_fence_before_sync();
   cluster_sync();   // the peer's barriers are initialised and both CTAs hold their TMEM columns
@@ -608,7 +612,7 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const C
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  grouped_gemm_kernel<EPI><<<num_sms(), THREADS, SMEM_BYTES, st>>>(ma, mb0, mb1, a);
+  MOE_RETURN_ON_ERROR(launch_k(grouped_gemm_kernel<EPI>, num_sms(), THREADS, SMEM_BYTES, st, ma, mb0, mb1, a));
   ++g_launches;
   return cudaGetLastError();
 }
@@ -623,16 +627,18 @@ static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, co
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = pair::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // the occupancy query below takes the cluster shape only
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pair::SMEM_BYTES);
@@ -646,6 +652,7 @@ static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, co
     configured_device = dev;
   }
   cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, ma, mb0, mb1, a);
   ++g_launches;
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const T* __restrict__ 
                                                           const float* __restrict__ lb, const float* __restrict__ sb,
                                                           int Tn, int d, int E, int k, int scoring, int32_t* idx,
                                                           float* gate, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= Tn) return;
@@ -224,6 +226,8 @@ __global__ void __launch_bounds__(256) route_vec_kernel(const T* __restrict__ x,
                                                         const float* __restrict__ lb, const float* __restrict__ sb,
                                                         int Tn, int d, int k, int scoring, int32_t* idx, float* gate,
                                                         uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VE = 16 / (int)sizeof(T);   // elements of d per 16-byte vector
   constexpr int NV = TW * E;                // partial logits per lane, index t * E + e
   constexpr int WG_VEC = E;                 // 16-byte vectors per VE rows of W_g (VE * E * sizeof(T) = 16 E)
@@ -317,6 +321,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ lb,
                                                          const float* __restrict__ sb, int Tn, int E, int k,
                                                          int scoring, int32_t* idx, float* gate, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= Tn) return;
@@ -346,6 +352,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 template <typename T>
 __global__ void __launch_bounds__(256) logits_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg, int Tn,
                                                           int d, int E, float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int BT = 64, BE = 64, BK = 16;
   __shared__ float xs[BK][BT + 4];
   __shared__ float ws[BK][BE + 4];
@@ -390,6 +398,8 @@ __global__ void __launch_bounds__(256) logits_simt_kernel(const T* __restrict__ 
 // Internals: A Systems Engineer's Field Manual", section 3.3).  Loads are compared in integers.
 __global__ void __launch_bounds__(256) update_sel_bias_kernel(const int32_t* __restrict__ counts, int E,
                                                               long long share, float gamma, float* sb) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const long long c = (long long)__ldg(counts + e) * E;
@@ -403,7 +413,8 @@ __global__ void __launch_bounds__(256) update_sel_bias_kernel(const int32_t* __r
 
 cudaError_t update_sel_bias(const int32_t* counts, int T, int k, int E, float gamma, float* sel_bias,
                             cudaStream_t st) {
-  update_sel_bias_kernel<<<(E + 255) / 256, 256, 0, st>>>(counts, E, (long long)T * k, gamma, sel_bias);
+  MOE_RETURN_ON_ERROR(launch_k(update_sel_bias_kernel, (E + 255) / 256, 256, 0, st, counts, E, (long long)T * k, gamma,
+                               sel_bias));
   ++g_launches;
   return cudaGetLastError();
 }
@@ -418,9 +429,9 @@ cudaError_t route_fused(int dtype, const void* x, const void* W_g, const float* 
     // tokens per block: enough to reuse each W_g vector, few enough to keep the partials in registers
     const int tw = E >= 32 ? 4 : E >= 8 ? 4 : 8;
     const unsigned blocks = (unsigned)((T + tw - 1) / tw);
-#define MOE_ROUTE_VEC(TY, EE, TWW)                                                                                \
-  route_vec_kernel<TY, EE, TWW><<<blocks, threads, 0, st>>>((const TY*)x, (const TY*)W_g, logit_bias, sel_bias, T, \
-                                                            d, k, scoring, idx, gate, err)
+#define MOE_ROUTE_VEC(TY, EE, TWW)                                                                           \
+  MOE_RETURN_ON_ERROR(launch_k(route_vec_kernel<TY, EE, TWW>, blocks, threads, 0, st, (const TY*)x, (const TY*)W_g, \
+                               logit_bias, sel_bias, T, d, k, scoring, idx, gate, err))
 #define MOE_ROUTE_VEC_E(TY)                          \
   switch (E) {                                       \
     case 1: MOE_ROUTE_VEC(TY, 1, 8); break;          \
@@ -441,9 +452,9 @@ cudaError_t route_fused(int dtype, const void* x, const void* W_g, const float* 
     return cudaGetLastError();
   }
   const unsigned blocks = (unsigned)(((long long)T * 32 + threads - 1) / threads);
-#define MOE_ROUTE_FUSED(TY, EM)                                                                                    \
-  route_fused_kernel<TY, EM><<<blocks, threads, 0, st>>>((const TY*)x, (const TY*)W_g, logit_bias, sel_bias, T, d, \
-                                                         E, k, scoring, idx, gate, err)
+#define MOE_ROUTE_FUSED(TY, EM)                                                                             \
+  MOE_RETURN_ON_ERROR(launch_k(route_fused_kernel<TY, EM>, blocks, threads, 0, st, (const TY*)x, (const TY*)W_g, \
+                               logit_bias, sel_bias, T, d, E, k, scoring, idx, gate, err))
   if (dtype == 1) {
     if (E <= 8) MOE_ROUTE_FUSED(uint16_t, 8);
     else if (E <= 16) MOE_ROUTE_FUSED(uint16_t, 16);
@@ -462,9 +473,11 @@ cudaError_t route_logits_simt(int dtype, const void* x, const void* W_g, int T, 
                               cudaStream_t st) {
   dim3 grid((E + 63) / 64, (T + 63) / 64);
   if (dtype == 1)
-    logits_simt_kernel<uint16_t><<<grid, 256, 0, st>>>((const uint16_t*)x, (const uint16_t*)W_g, T, d, E, logits);
+    MOE_RETURN_ON_ERROR(launch_k(logits_simt_kernel<uint16_t>, grid, 256, 0, st, (const uint16_t*)x, (const uint16_t*)W_g,
+                                 T, d, E, logits));
   else
-    logits_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)x, (const float*)W_g, T, d, E, logits);
+    MOE_RETURN_ON_ERROR(launch_k(logits_simt_kernel<float>, grid, 256, 0, st, (const float*)x, (const float*)W_g, T, d, E,
+                                 logits));
   ++g_launches;
   return cudaGetLastError();
 }
@@ -473,8 +486,9 @@ cudaError_t route_topk(const float* logits, const float* logit_bias, const float
                        int scoring, int32_t* idx, float* gate, uint32_t* err, cudaStream_t st) {
   const int threads = 256;
   const unsigned blocks = (unsigned)(((long long)T * 32 + threads - 1) / threads);
-#define MOE_TOPK(EPL) \
-  route_topk_kernel<EPL><<<blocks, threads, 0, st>>>(logits, logit_bias, sel_bias, T, E, k, scoring, idx, gate, err)
+#define MOE_TOPK(EPL)                                                                                       \
+  MOE_RETURN_ON_ERROR(launch_k(route_topk_kernel<EPL>, blocks, threads, 0, st, (const float*)logits, logit_bias, \
+                               sel_bias, T, E, k, scoring, idx, gate, err))
   if (E <= 32) MOE_TOPK(1);
   else if (E <= 64) MOE_TOPK(2);
   else if (E <= 128) MOE_TOPK(4);

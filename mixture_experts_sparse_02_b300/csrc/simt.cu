@@ -32,6 +32,8 @@ struct SimtArgs {
 template <int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ W0,
                                                         const float* __restrict__ W1, const SimtArgs p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[BK][BM + 4];
   __shared__ float B0s[BK][BN + 4];
   __shared__ float B1s[EPI == EPI_SWIGLU ? BK : 1][BN + 4];
@@ -119,7 +121,7 @@ cudaError_t launch(const float* A, const float* W0, const float* W1, const SimtA
   const long long row_tiles = p.offsets ? ((long long)p.rows_cap + BM - 1) / BM + p.G : ((long long)p.M + BM - 1) / BM;
   if (row_tiles <= 0) return cudaSuccess;
   dim3 grid((p.N + BN - 1) / BN, (unsigned)row_tiles);
-  simt_gemm_kernel<EPI><<<grid, 256, 0, st>>>(A, W0, W1, p);
+  MOE_RETURN_ON_ERROR(launch_k(simt_gemm_kernel<EPI>, grid, 256, 0, st, A, W0, W1, p));
   ++g_launches;
   return cudaGetLastError();
 }

@@ -27,6 +27,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256) score_partial_kernel(const float* __restrict__ logits,
                                                             const float* __restrict__ lb, int T, int E, int scoring,
                                                             int tokens_per_block, float* __restrict__ partial) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8][EPL * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * tokens_per_block;
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float* __restri
                                                            const int32_t* __restrict__ counts, int T, int k, int E,
                                                            float alpha, float* __restrict__ f, float* __restrict__ P,
                                                            float* __restrict__ summary) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float prod[1024];
   __shared__ int cmax[1024];
   const int e = threadIdx.x;
@@ -125,8 +129,9 @@ cudaError_t load_stats(const float* logits, const float* logit_bias, const int32
                        cudaStream_t st) {
   const int tpb = max(8, (T + 295) / 296);
   const int nblk = (T + tpb - 1) / tpb;
-#define MOE_SCORE_PARTIAL(EPL)                                                                                \
-  score_partial_kernel<EPL><<<nblk, 256, 0, st>>>(logits, logit_bias, T, E, scoring, tpb, partial)
+#define MOE_SCORE_PARTIAL(EPL)                                                                          \
+  MOE_RETURN_ON_ERROR(launch_k(score_partial_kernel<EPL>, nblk, 256, 0, st, logits, logit_bias, T, E, scoring, tpb, \
+                               partial))
   if (E <= 32) MOE_SCORE_PARTIAL(1);
   else if (E <= 64) MOE_SCORE_PARTIAL(2);
   else if (E <= 128) MOE_SCORE_PARTIAL(4);
@@ -137,7 +142,8 @@ cudaError_t load_stats(const float* logits, const float* logit_bias, const int32
   ++g_launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  stats_final_kernel<<<1, 1024, 0, st>>>(partial, nblk, counts, T, k, E, alpha, f, P, summary);
+  MOE_RETURN_ON_ERROR(launch_k(stats_final_kernel, 1, 1024, 0, st, (const float*)partial, nblk, counts, T, k, E, alpha,
+                               f, P, summary));
   ++g_launches;
   return cudaGetLastError();
 }
