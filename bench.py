@@ -41,8 +41,8 @@ FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM on the default workload, from
 # one ncu capture of a half-size case scaled to the full launch (profiles/), per kernel
 # variant, valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"source_sha256": "25f7aeaa4f5461994945df46e3fe2596650a2466da3f5d93124ca6efb2c5eada",
-               "bytes_per_launch": {"pair": 2206.4e6}}
+NCU_TRAFFIC = {"source_sha256": "979027cbcfbb88699a972559b16c5e1bd2c5cad351f2974d826bc326ae5979c9",
+               "bytes_per_launch": {"pair": 2202.3e6}}
 
 
 def _sha256(path):
@@ -243,11 +243,11 @@ def traffic_for_kernel(variant):
 
 
 def gemm_variant(shape):
-    """Which grouped-GEMM kernel the library runs for the routed experts of this workload:
-    the same rule as the library (CTA pairs when groups average >= 512 rows, unless
+    """Which grouped-GEMM kernel the library runs for the routed W1/W2 + SwiGLU GEMM of this
+    workload: the library's rule (CTA pairs when expert blocks average >= 512 rows, unless
     MOE_GEMM_KERNEL forces one)."""
     forced = os.environ.get("MOE_GEMM_KERNEL")
-    if forced in ("single", "pair"):
+    if forced in ("single", "pair", "tpair"):
         return forced
     return "pair" if shape.T * shape.k >= 512 * shape.E else "single"
 
@@ -318,7 +318,8 @@ def run_ours(args, shape, world, rank, local):
     peak = pk["bf16_tflops"]
     ach = fl_w12 / t_w12 / 1e12
     variant = gemm_variant(shape)
-    kname = "grouped_gemm_pair_kernel<EPI_SWIGLU>" if variant == "pair" else "grouped_gemm_kernel<EPI_SWIGLU>"
+    kname = {"pair": "grouped_gemm_pair_kernel", "tpair": "grouped_gemm_tpair_kernel"}.get(
+        variant, "grouped_gemm_kernel") + "<EPI_SWIGLU>"
     roof = {"bound": "tensor", "kernel": kname + " (W1/W2 + SiLU*mul)",
             "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
             "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(variant),

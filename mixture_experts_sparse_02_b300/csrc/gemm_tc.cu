@@ -552,6 +552,269 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   }
 }
 
+// ------------------------------------------------------------------------- token-wide CTA-pair kernel
+// The CTA-pair GEMM with the operands' roles swapped: the weights' output features run along the
+// MMA's M (256 per pair, 128 per CTA) and the tokens along its N.  N is chosen per tile, in steps
+// of 16 up to 256, so the last tile of an expert's block carries at most 15 rows of padding
+// (with tokens along M the padding reaches 255 rows per expert, about a tenth of the work on
+// the Mixtral-shaped layer).
+//   A (MMA M, weights, MN-major): per CTA and stage two 64-feature x 64-k boxes.  SWIGLU: box 0
+//     is W1 for features f0 + 64 r .. + 63 and box 1 is W2 for the same features, so a CTA's
+//     TMEM lanes 0-63 hold X W1 and lanes 64-127 hold X W2 of the same 64 features; EPI_F32:
+//     the two boxes are output features f0 + 128 r .. + 127.
+//   B (MMA N, tokens, K-major): CTA r loads the 128-row box at token row0 + r N / 2; the MMA
+//     takes N / 2 rows from each CTA.
+// The SwiGLU epilogue passes X W2 from the warps that hold it (lanes 64-127) to the warps that
+// hold X W1 of the same features through a small shared-memory buffer, 32 tokens at a time.
+// Synchronisation is that of the pair kernel above.
+namespace tpair {
+constexpr int TOK = 256;                           // tokens per pair tile (MMA N)
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 2 * B_SUB;                 // 16 KB
+constexpr int B_BYTES = BM * BK * 2;               // 16 KB: 128 token rows x 64 k
+constexpr int STAGE = A_BYTES + B_BYTES;           // 32 KB
+constexpr int XCHG_FLOATS = 2 * 32 * 32;           // X W2 of 64 features x 32 tokens
+constexpr uint32_t IDESC_BASE = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(256 >> 4) << 24);
+
+// Instruction descriptor: D f32, A and B bf16, A MN-major, B K-major, M = 256, N = n.
+__host__ __device__ __forceinline__ uint32_t idesc(int n) { return IDESC_BASE | ((uint32_t)(n >> 3) << 17); }
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  int ep_ok[4];
+  int tile_start[MAX_GROUPS + 1];
+  int row_off[MAX_GROUPS + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + XCHG_FLOATS * 4 + sizeof(Ctrl);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+}  // namespace tpair
+
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+                          const __grid_constant__ CUtensorMap tmW1, const GemmArgs a) {
+  using tpair::STAGES;
+  using tpair::STAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* xchg = reinterpret_cast<float*>(smem + (size_t)STAGES * STAGE);
+  tpair::Ctrl& c = *reinterpret_cast<tpair::Ctrl*>(smem + (size_t)STAGES * STAGE + tpair::XCHG_FLOATS * 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.offsets ? a.G : 1;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = (int)(blockIdx.x >> 1);
+  const int nclusters = (int)(gridDim.x >> 1);
+  const int feat_per_tile = EPI == EPI_SWIGLU ? 128 : 256;   // output features of one pair tile
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.tfull[b], 1);
+      mbar_init(&c.tempty[b], 8);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort = 0;
+    fence_barrier_init_cluster();
+    fence_proxy_async_smem();
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW0);
+    prefetch_tensormap(&tmW1);
+  }
+  if (warp == 2) tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+  pdl_wait();      // offsets, rows and the outputs belong to earlier kernels of the stream
+  pdl_trigger();
+  if (warp == 3) build_group_table<tpair::TOK>(c, a, G, lane);
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+
+  const uint32_t tmem = c.tmem_base;
+  const int total = c.tile_start[G];
+  const int num_kb = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      int s = 0;
+      uint32_t phase = 0;
+      for (int t = a.starve ? total : cid; t < total; t += nclusters) {
+        const Tile tl = decode_tile<tpair::TOK>(c, G, t);
+        const int z = a.offsets ? tl.g : a.b_z;
+        const int rows = min(tpair::TOK, tl.row_end - tl.row0);
+        const int n_mma = (rows + 15) & ~15;
+        const int trow = tl.row0 + (int)rank * (n_mma >> 1);
+        const int fa = tl.n_tile * feat_per_tile + (EPI == EPI_SWIGLU ? 64 : 128) * (int)rank;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort, a.wait_limit_ns)) {
+            flag_error(a.err, ERR_WAIT_PRODUCER);
+            c.abort = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + (size_t)s * STAGE;
+          uint8_t* sb = sa + tpair::A_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&c.full[s], 2 * STAGE);
+          const uint32_t fb = mapa_shared(smem_addr(&c.full[s]), 0);
+          const int k0 = kb * BK;
+          if (EPI == EPI_SWIGLU) {
+            tma_load_3d_pair(sa, &tmW0, fb, fa, k0, z);
+            tma_load_3d_pair(sa + B_SUB, &tmW1, fb, fa, k0, z);
+          } else {
+            tma_load_3d_pair(sa, &tmW0, fb, fa, k0, z);
+            tma_load_3d_pair(sa + B_SUB, &tmW0, fb, fa + 64, k0, z);
+          }
+          tma_load_2d_pair(sb, &tmX, fb, k0, trow);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (CTA 0)
+      int s = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += nclusters, ++it) {
+        const Tile tl = decode_tile<tpair::TOK>(c, G, t);
+        const int rows = min(tpair::TOK, tl.row_end - tl.row0);
+        const uint32_t idesc = tpair::idesc((rows + 15) & ~15);
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort, a.wait_limit_ns)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
+          const uint32_t sb = sa + tpair::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K
+            // step of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.
+            const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+          }
+          umma_commit_pair(&c.empty[s], 0x3);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&c.tfull[buf], 0x3);
+      }
+      if (!ok) {
+        flag_error(a.err, ERR_WAIT_MMA);
+        c.abort = 1;
+        umma_commit_pair(&c.drain, 0x1);
+        volatile int never = 0;
+        mbar_wait(&c.drain, 0, &never, a.wait_limit_ns);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;   // TMEM lanes 32 q .. 32 q + 31
+    const uint32_t tempty0 = mapa_shared(smem_addr(&c.tempty[0]), 0);
+    const uint32_t tempty1 = mapa_shared(smem_addr(&c.tempty[1]), 0);
+    int it = 0;
+    for (int t = cid; t < total; t += nclusters, ++it) {
+      const Tile tl = decode_tile<tpair::TOK>(c, G, t);
+      const int rows = min(tpair::TOK, tl.row_end - tl.row0);
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      // the four epilogue warps take the same decision (they meet at named barriers below)
+      const bool mine = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort, a.wait_limit_ns));
+      if (lane == 0) c.ep_ok[q] = mine ? 1 : 0;
+      epilogue_bar();
+      const bool got = c.ep_ok[0] && c.ep_ok[1] && c.ep_ok[2] && c.ep_ok[3];
+      epilogue_bar();
+      if (!got) {
+        if (lane == 0 && !mine) flag_error(a.err, ERR_WAIT_EPILOGUE);
+        c.abort = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (EPI == EPI_SWIGLU) {
+        // lanes 0-63: X W1, lanes 64-127: X W2, for features fbase .. fbase + 63
+        const int fbase = tl.n_tile * 128 + 64 * (int)rank;
+        const int f = fbase + 32 * (q & 1) + lane;
+        float* xv = xchg + (q & 1) * 32 * 32;
+        uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
+        for (int col0 = 0; col0 < rows; col0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + col0, r);
+          tmem_ld_wait();
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xv[j * 32 + lane] = __uint_as_float(r[j]);
+          }
+          epilogue_bar();
+          if (q < 2 && f < a.N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < rows) {
+                const float u = __uint_as_float(r[j]);
+                const float v = xv[j * 32 + lane];
+                const float h = u * __fdividef(v, 1.0f + __expf(-v));
+                out[(size_t)(tl.row0 + col0 + j) * a.ldo + f] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+              }
+            }
+          }
+          epilogue_bar();
+        }
+      } else {
+        const int f = tl.n_tile * 256 + 128 * (int)rank + 32 * q + lane;
+        float* out = reinterpret_cast<float*>(a.out);
+        for (int col0 = 0; col0 < rows; col0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + col0, r);
+          tmem_ld_wait();
+          if (f < a.N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < rows) {
+                float* dst = out + (size_t)(tl.row0 + col0 + j) * a.ldo + f;
+                const float v = __uint_as_float(r[j]);
+                *dst = a.accumulate ? *dst + v : v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && c.abort) settle_after_abort();
+  tc_fence_before_sync();
+  cluster_sync();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------------- host side
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -618,12 +881,16 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const C
 }
 
 // Persistent grid of CTA pairs: as many clusters of 2 as can be resident at once (at most
-// half the SMs).
-template <int EPI>
-static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
-                               const GemmArgs& a, cudaStream_t st) {
-  static int configured_device = -1;
-  static int clusters = 0;
+// half the SMs).  `slot` caches the per-kernel configuration.
+struct PairLaunchCache {
+  int device = -1;
+  int clusters = 0;
+};
+
+template <typename Kernel>
+static cudaError_t launch_cluster_pair(Kernel kernel, size_t smem, PairLaunchCache& cache, const CUtensorMap& m0,
+                                       const CUtensorMap& m1, const CUtensorMap& m2, const GemmArgs& a,
+                                       cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
@@ -635,27 +902,40 @@ static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, co
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;   // the occupancy query below takes the cluster shape only
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)pair::SMEM_BYTES);
+  cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+  if (cache.device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int n = 0;
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
-    clusters = n < num_sms() / 2 ? n : num_sms() / 2;
-    configured_device = dev;
+    cache.clusters = n < num_sms() / 2 ? n : num_sms() / 2;
+    cache.device = dev;
   }
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.gridDim = dim3(2 * cache.clusters, 1, 1);
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, ma, mb0, mb1, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, m2, a);
   ++g_launches;
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int EPI>
+static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
+                               const GemmArgs& a, cudaStream_t st) {
+  static PairLaunchCache cache;
+  return launch_cluster_pair(grouped_gemm_pair_kernel<EPI>, pair::SMEM_BYTES, cache, ma, mb0, mb1, a, st);
+}
+
+template <int EPI>
+static cudaError_t launch_tpair(const CUtensorMap& mx, const CUtensorMap& mw0, const CUtensorMap& mw1,
+                                const GemmArgs& a, cudaStream_t st) {
+  static PairLaunchCache cache;
+  return launch_cluster_pair(grouped_gemm_tpair_kernel<EPI>, tpair::SMEM_BYTES, cache, mx, mw0, mw1, a, st);
 }
 
 // Test hook: one starved launch with a short wait limit (moe_test_pipeline_fault).
@@ -671,15 +951,26 @@ static void apply_test_hook(GemmArgs& a) {
   }
 }
 
-// Kernel choice: "pair" tiles are 256 rows, so they pay off when groups are large; the
-// single-CTA kernel (128-row tiles) wastes fewer rows on small or ragged groups.  The
-// environment variable MOE_GEMM_KERNEL=single|pair overrides the choice (used by the tests to
-// run both kernels on the same inputs).
-static bool use_pair(long long rows, int groups) {
+// Kernel choice, from measurements on B300 (Mixtral-, Hunyuan- and DeepSeek-V3-shaped layers):
+//   W1/W2 + SwiGLU: the CTA-pair kernel ("pair", 256 token rows per tile) for expert blocks
+//     that average >= 512 rows, else the single-CTA kernel (128-row tiles).  The token-wide pair
+//     kernel is no faster here: its short tail tiles still stream the whole weight slice, and its
+//     epilogue has to pass X W2 between warps.
+//   float32 outputs (W3, router logits): the token-wide CTA-pair kernel ("tpair", tokens along
+//     N in steps of 16) for blocks that average >= 128 rows, else the single-CTA kernel.
+// Decode-sized batches (a few rows per expert) take the single-CTA kernel, which streams each
+// expert's weights once with the fewest bytes per row.  MOE_GEMM_KERNEL=single|pair|tpair
+// overrides the choice (the tests run every kernel on the same inputs).
+enum Variant { V_SINGLE = 0, V_PAIR = 1, V_TPAIR = 2 };
+
+static Variant choose_variant(int epi, long long rows, int groups) {
   const char* v = getenv("MOE_GEMM_KERNEL");
-  if (v && strcmp(v, "single") == 0) return false;
-  if (v && strcmp(v, "pair") == 0) return true;
-  return rows >= 512LL * (groups > 0 ? groups : 1);
+  if (v && strcmp(v, "single") == 0) return V_SINGLE;
+  if (v && strcmp(v, "pair") == 0) return V_PAIR;
+  if (v && strcmp(v, "tpair") == 0) return V_TPAIR;
+  const long long g = groups > 0 ? groups : 1;
+  if (epi == EPI_SWIGLU) return rows >= 512LL * g ? V_PAIR : V_SINGLE;
+  return rows >= 128LL * g ? V_TPAIR : V_SINGLE;
 }
 
 }  // namespace tc
@@ -697,12 +988,14 @@ cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, 
     return cudaErrorInvalidValue;
   GemmArgs a{};
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
-  a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);
+  a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);   // 128 output columns per tile (all variants)
   a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
-  if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
-    return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
-  return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+  switch (tc::choose_variant(EPI_SWIGLU, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
+    case tc::V_TPAIR: return tc::launch_tpair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+    case tc::V_PAIR: return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+    default: return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+  }
 }
 
 // out[rows, N] (f32) (+)= A W, grouped.  A is [rows_cap, K] bf16; W is [Z][K][N] bf16.
@@ -713,12 +1006,14 @@ cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* 
   if (!tc::make_map_a(&ma, A, rows_cap, K) || !tc::make_map_b(&mb, W, Z, K, N)) return cudaErrorInvalidValue;
   GemmArgs a{};
   a.offsets = offsets; a.G = G; a.M = M_dense; a.K = K; a.N = N;
-  a.n_tiles = (N + tc::BN - 1) / tc::BN;
+  a.n_tiles = (N + tc::BN - 1) / tc::BN;             // 256 output columns per tile (all variants)
   a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
-  if (tc::use_pair(offsets ? rows_cap : M_dense, offsets ? G : 1))
-    return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
-  return tc::launch<EPI_F32>(ma, mb, mb, a, st);
+  switch (tc::choose_variant(EPI_F32, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
+    case tc::V_TPAIR: return tc::launch_tpair<EPI_F32>(ma, mb, mb, a, st);
+    case tc::V_PAIR: return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
+    default: return tc::launch<EPI_F32>(ma, mb, mb, a, st);
+  }
 }
 
 }  // namespace moe

@@ -38,9 +38,10 @@ SMALL = [
     S("f32_e2", T=90, d=64, d_ff=32, E=2, k=1, dtype="f32", scoring="sigmoid"),
 ]
 
-# Shapes for running both grouped-GEMM kernels (128-row single-CTA tiles, 256-row CTA-pair
-# tiles) on the same inputs: ragged groups that end inside a tile, empty experts, a group
-# larger than one pair tile, N not a multiple of the tile width, shared experts accumulating.
+# Shapes for running every grouped-GEMM kernel (128-row single-CTA tiles, 256-row CTA-pair
+# tiles, token-wide CTA-pair tiles of 16..256 tokens) on the same inputs: ragged groups that end
+# inside a tile, empty experts, a group larger than one pair tile, N not a multiple of the tile
+# width, shared experts accumulating.
 GEMM_SHAPES = [
     S("gemm_ragged_e6", T=1000, d=512, d_ff=776, E=6, k=2, dtype="bf16", scoring="softmax", logit_bias_std=1.0),
     S("gemm_skewed_e64", T=257, d=256, d_ff=320, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.5),
@@ -142,10 +143,10 @@ def test_stages_small(moe, shape):
     assert moe.get_device_error() == 0
 
 
-@pytest.mark.parametrize("variant", ["single", "pair"])
+@pytest.mark.parametrize("variant", ["single", "pair", "tpair"])
 @pytest.mark.parametrize("shape", GEMM_SHAPES, ids=[s.name for s in GEMM_SHAPES])
 def test_gemm_kernels(moe, shape, variant, monkeypatch):
-    """Both grouped-GEMM kernels, forced, against the oracle: the experts call alone (oracle
+    """Each grouped-GEMM kernel, forced, against the oracle: the experts call alone (oracle
     x_perm and offsets in) and the whole layer; results are run-to-run identical."""
     monkeypatch.setenv("MOE_GEMM_KERNEL", variant)
     s = shape
