@@ -125,3 +125,40 @@ def test_capacity_nobody_reaches_changes_nothing(moe):
         moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb)
         out.append(y)
     assert torch.equal(out[0], out[1])
+
+
+def test_capacity_full_size_hunyuan_shaped(moe):
+    """The skewed 64-expert layer at full size with a capacity factor of 1.25: every routing and
+    dispatch output bit-exact, and sampled tokens (including ones that lost an expert) against
+    the definition."""
+    s = wl.WORKLOADS["hunyuan_a13b"].replace(capacity_factor=1.25)
+    case = Case(s, 0)
+    r = case.route()
+    slots = orc.capacity_slots(s.T, s.k, s.E, s.capacity_factor)
+    dsp = orc.dispatch(r["idx"], s.E, slots)
+    dropped_tok = np.nonzero((dsp["inv_pos"] == -1).any(axis=1))[0]
+    assert dropped_tok.size > 0
+    rng = np.random.default_rng(3)
+    sample = np.unique(np.concatenate([dropped_tok[:6], rng.choice(s.T, 10, replace=False), [0, s.T - 1]]))
+    W = upload_experts(s, 0, keep=np.unique(r["idx"][sample]))
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    lb = torch.from_numpy(case.logit_bias).cuda()
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb, topk_idx_out=idx, counts_out=counts)
+    assert moe.get_device_error() == 0
+    assert np.array_equal(idx.cpu().numpy(), r["idx"])
+    assert np.array_equal(counts.cpu().numpy(), dsp["counts"])
+    b = _dispatch_buffers(s)
+    moe.dispatch(cfg, idx, x, b["counts"], b["offsets"], b["perm"], b["inv"], b["x_perm"], ws)
+    assert np.array_equal(b["offsets"].cpu().numpy(), dsp["offsets"])
+    assert np.array_equal(b["inv"].cpu().numpy(), dsp["inv_pos"])
+    kept = int(dsp["offsets"][-1])
+    assert np.array_equal(b["perm"][:kept].cpu().numpy(), dsp["perm_tok"])
+    get_w = lambda name, e: wl.to_f64(W["host"][(name, e)], s.dtype)
+    y_ref = orc.forward_tokens(case.f64(case.x[sample]), r["idx"][sample], r["gate"][sample], get_w, 0,
+                               kept_rows=dsp["inv_pos"][sample] >= 0)
+    assert layer_out_err(dev_to_f64(y[torch.from_numpy(sample).cuda()]), y_ref, s) <= y_tol(s)

@@ -89,3 +89,39 @@ def test_expert_choice_rejects_token_choice_calls(moe):
     with pytest.raises(moe.MoEError) as e:
         moe.forward(cfg, fake, fake, fake, fake, fake, fake, fake, ws_bytes=1 << 40, topk_idx_out=fake, stream=0)
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_expert_choice_full_size_mixtral_shaped(moe):
+    """Expert choice on the Mixtral-shaped layer at full size (T = 4096, each of the 8 experts
+    takes 1024 tokens): the routing bit-exact, sampled tokens against the definition."""
+    s = wl.WORKLOADS["mixtral_prefill"].replace(scoring="expert_choice")
+    case = Case(s, 0)
+    m = case.ec_m
+    r = orc.expert_choice_route(case.f64(case.x), case.f64(case.W_g), s.E, m, case.logit_bias)
+    took = (r["pos_of"] >= 0).sum(axis=1)
+    rng = np.random.default_rng(4)
+    sample = np.unique(np.concatenate([np.nonzero(took == 0)[0][:3], np.nonzero(took == took.max())[0][:3],
+                                       rng.choice(s.T, 10, replace=False)]))
+    W = upload_experts(s, 0, keep=range(s.E))
+    x, Wg = to_dev(case.x, s), to_dev(case.W_g, s)
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.empty((s.E * m,), dtype=torch.int32, device="cuda")
+    gate = torch.empty((s.E * m,), dtype=torch.float32, device="cuda")
+    pos_of = torch.empty((s.T, s.E), dtype=torch.int32, device="cuda")
+    moe.route_expert_choice(cfg, x, Wg, offsets, perm, gate, pos_of, ws=ws)
+    assert np.array_equal(perm.cpu().numpy(), r["perm_tok"])
+    assert np.array_equal(pos_of.cpu().numpy(), r["pos_of"])
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws)
+    assert moe.get_device_error() == 0
+    get_w = lambda name, e: wl.to_f64(W["host"][(name, e)], s.dtype)
+    xs = case.f64(case.x[sample])
+    y_ref = np.zeros((len(sample), s.d))
+    for e in range(s.E):
+        rows = np.nonzero(r["pos_of"][sample, e] >= 0)[0]
+        if rows.size:
+            fe = orc.swiglu_expert(xs[rows], get_w("W1", e), get_w("W2", e), get_w("W3", e))
+            y_ref[rows] += r["scores"][sample[rows], e][:, None] * fe
+    assert layer_out_err(dev_to_f64(y[torch.from_numpy(sample).cuda()]), y_ref, s) <= y_tol(s)
