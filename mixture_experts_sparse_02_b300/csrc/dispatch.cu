@@ -17,6 +17,8 @@
 //            for that expert plus its rank among the lanes of the same expert in that round.
 //            Pairs of one expert therefore keep ascending i.
 //   gather   x_perm[p] = x[perm_tok[p]], one warp per row with 16-byte vector copies.
+// Batches of up to 4096 pairs over at most 256 experts take one single-block kernel for the
+// first three steps instead (dispatch_small_kernel).
 #include "common.cuh"
 #include "internal.h"
 
@@ -194,6 +196,109 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
   }
 }
 
+// Small batches (T k <= SMALL_PAIRS, E <= SMALL_E), as decode steps produce: the histogram,
+// scan and permutation in one block of 1024 threads, with the same results as the three
+// kernels above.  Rounds of 1024 pairs in flattened order; warp w of a round takes its 32
+// pairs; a pair's rank within its expert is (pairs of the expert in earlier rounds) + (in
+// earlier warps of the round) + (lanes of its warp before it with the same expert).
+constexpr int SMALL_PAIRS = 4096;
+constexpr int SMALL_E = 256;
+
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __restrict__ idx, int N, int k, int E,
+                                                              int cap, int32_t* __restrict__ counts,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ perm_tok,
+                                                              int32_t* __restrict__ inv_pos, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int wc[32][SMALL_E];   // per-warp counts of a round, then their exclusive prefix over warps
+  __shared__ int run[SMALL_E];      // per-expert totals, then pairs of each expert in earlier rounds
+  __shared__ int off[SMALL_E + 1];
+  __shared__ int wsum[33];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += 1024) run[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int i = tid; i < N; i += 1024) {
+    const int e = __ldg(idx + i);
+    if (e < 0 || e >= E) bad = true;
+    else atomicAdd(&run[e], 1);   // counts only: the order of these additions does not matter
+  }
+  if (bad) flag_error(err, ERR_EXPERT_ID);
+  __syncthreads();
+  // exclusive scan of the kept counts over the experts (E <= 256 < 1024 threads)
+  const int kept = tid < E ? min(run[tid], cap) : 0;
+  int incl = kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = wsum[lane];
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(FULL, xi, o);
+      if (lane >= o) xi += n;
+    }
+    wsum[lane] = xi - x;
+    if (lane == 31) wsum[32] = xi;
+  }
+  __syncthreads();
+  const int excl = incl - kept + wsum[warp];
+  if (tid < E) {
+    counts[tid] = run[tid];
+    off[tid] = excl;
+    offsets[tid] = excl;
+  }
+  if (tid == 0) {
+    off[E] = wsum[32];
+    offsets[E] = wsum[32];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) run[e] = 0;
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = 0; base < N; base += 1024) {
+    const int i = base + tid;
+    int e = -1;
+    if (i < N) {
+      e = __ldg(idx + i);
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned m = __match_any_sync(FULL, e);
+    for (int x = lane; x < E; x += 32) wc[warp][x] = 0;
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) wc[warp][e] = __popc(m);
+    __syncthreads();
+    for (int x = tid; x < E; x += 1024) {
+      int r = run[x];
+      for (int w = 0; w < 32; ++w) {
+        const int c = wc[w][x];
+        wc[w][x] = r;
+        r += c;
+      }
+      run[x] = r;
+    }
+    __syncthreads();
+    if (i < N) {
+      int pos = -1;
+      if (e >= 0) {
+        const int rank = wc[warp][e] + __popc(m & lt);
+        if (rank < cap) {
+          pos = off[e] + rank;
+          perm_tok[pos] = (int32_t)(i / k);
+        }
+      }
+      inv_pos[i] = pos;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 int dispatch_num_chunks(long long pairs) { return (int)((pairs + CHUNK - 1) / CHUNK); }
@@ -202,6 +307,13 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int c
                              int32_t* chunk_base, int32_t* counts, int32_t* offsets, int32_t* perm_tok,
                              int32_t* inv_pos, uint32_t* err, cudaStream_t st, int* launches) {
   const long long N = (long long)T * k;
+  if (N <= SMALL_PAIRS && E <= SMALL_E) {
+    MOE_RETURN_ON_ERROR(launch_k(dispatch_small_kernel, 1, 1024, 0, st, topk_idx, (int)N, k, E, cap, counts, offsets,
+                                 perm_tok, inv_pos, err));
+    g_launches += 1;
+    if (launches) *launches += 1;
+    return cudaGetLastError();
+  }
   const int n_chunks = dispatch_num_chunks(N);
   const unsigned blocks = (unsigned)((n_chunks + WARPS - 1) / WARPS);
   const size_t shm = (size_t)WARPS * E * sizeof(int);

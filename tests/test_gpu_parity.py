@@ -78,8 +78,10 @@ def _forward(moe, case, W, din):
 
 def _expected_launches(s):
     """Kernels one moe_forward launches: router (logits + top-k when E > 32), dispatch (histogram,
-    scan, permute, gather), W1/W2, W3, two per shared expert, combine."""
-    return (1 if s.E <= 32 else 2) + 4 + 2 + 2 * s.n_shared + 1
+    scan, permute, gather; one kernel for the first three up to 4096 pairs over <= 256 experts),
+    W1/W2, W3, two per shared expert, combine."""
+    small = s.T * s.k <= 4096 and s.E <= 256
+    return (1 if s.E <= 32 else 2) + (2 if small else 4) + 2 + 2 * s.n_shared + 1
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
