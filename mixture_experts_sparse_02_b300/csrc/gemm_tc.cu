@@ -5,23 +5,32 @@
 // one dense matmul; page "8.6 - Mixture of Experts (MoE)", section 2: the SwiGLU expert).
 //
 // Two epilogues:
-//   EPI_SWIGLU  h = (X W1) * SiLU(X W2), written as bf16.  One 128 x 256 MMA tile holds
-//               128 columns of X W1 next to the same 128 columns of X W2, so the pair is
-//               finished in registers without a round trip through memory.
+//   EPI_SWIGLU  h = (X W1) * SiLU(X W2), written as bf16.  An accumulator tile holds X W1 and
+//               X W2 for the same output columns, so the pair is finished on chip.
 //   EPI_F32     out (+)= X W, written as float32 (expert W3, shared W3, router logits).
 //
-// Work decomposition: a persistent grid of one CTA per SM walks the tiles
-// (group, n-tile, m-tile) in that order (m fastest, so CTAs that run at the same time share
-// one weight tile and the weights are streamed from HBM about once).  Group sizes are read on
-// the device from `offsets`, so nothing is synchronised with the host.  Row tiles may run
-// past the end of their group: the extra rows belong to the next group (or lie beyond the
-// matrix and are zero-filled by TMA) and their results are not stored.
+// Three kernels, all persistent (one CTA per SM, or one CTA pair per two SMs), all reading the
+// group sizes on the device from `offsets` (nothing is synchronised with the host):
+//   grouped_gemm_kernel        1 CTA, 128 token rows x 256 MMA columns per tile, 4 x 48 KB
+//                              stages.  For small expert blocks (decode) and ragged ones.
+//   grouped_gemm_pair_kernel   a cluster of 2 CTAs shares one tcgen05.mma.cta_group::2 of
+//                              256 token rows x 256 columns; each CTA loads its 128 rows and
+//                              half of the weight columns; 6 x 32 KB stages.  W1/W2 + SwiGLU
+//                              for blocks averaging >= 512 rows.
+//   grouped_gemm_tpair_kernel  the CTA pair with the roles swapped: weight features along the
+//                              MMA's M (256), tokens along N in steps of 16 up to 256, so the
+//                              last tile of a block carries at most 15 padding rows.  The
+//                              float32-output GEMMs for blocks averaging >= 128 rows.
+// Tiles are walked as (group, column tile, row tile), row tiles fastest, so the CTAs that run
+// at the same time share one weight tile and the weights are streamed from HBM about once.
+// Row tiles may run past the end of their group: the extra rows belong to the next group (or
+// lie beyond the matrix and are zero-filled by TMA) and their results are not stored.
 //
-// Warp roles (256 threads): warp 0 lane 0 issues TMA loads into a 4-stage shared-memory
-// ring; warp 1 lane 0 issues tcgen05.mma into one of two 256-column TMEM accumulators;
-// warps 4-7 drain the other accumulator (tcgen05.ld) and store; warp 2 owns the TMEM
-// allocation; warp 3 builds the group table.  Every wait is bounded (kWaitLimitNs) and on a
-// timeout sets the device error word and unwinds.
+// Warp roles (256 threads): warp 0 lane 0 issues the TMA loads into the shared-memory ring;
+// warp 1 lane 0 issues tcgen05.mma into one of two 256-column TMEM accumulators; warps 4-7
+// drain the other accumulator (tcgen05.ld) and store; warp 2 owns the TMEM allocation; warp 3
+// builds the group table.  Every wait is bounded (kWaitLimitNs, or a test hook's shorter
+// limit) and on a timeout sets the device error word and unwinds.
 #include <cudaTypedefs.h>
 #include <atomic>
 #include <stdlib.h>
