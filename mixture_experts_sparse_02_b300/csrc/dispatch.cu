@@ -17,7 +17,7 @@
 //            for that expert plus its rank among the lanes of the same expert in that round.
 //            Pairs of one expert therefore keep ascending i.
 //   gather   x_perm[p] = x[perm_tok[p]], one warp per row with 16-byte vector copies.
-// Batches of up to 4096 pairs over at most 256 experts take one single-block kernel for the
+// Batches of up to 16384 pairs over at most 256 experts take one single-block kernel for the
 // first three steps instead (dispatch_small_kernel).
 #include "common.cuh"
 #include "internal.h"
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
 // kernels above.  Rounds of 1024 pairs in flattened order; warp w of a round takes its 32
 // pairs; a pair's rank within its expert is (pairs of the expert in earlier rounds) + (in
 // earlier warps of the round) + (lanes of its warp before it with the same expert).
-constexpr int SMALL_PAIRS = 4096;
+constexpr int SMALL_PAIRS = 16384;
 constexpr int SMALL_E = 256;
 
 __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __restrict__ idx, int N, int k, int E,

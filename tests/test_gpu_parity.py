@@ -78,9 +78,9 @@ def _forward(moe, case, W, din):
 
 def _expected_launches(s):
     """Kernels one moe_forward launches: router (logits + top-k when E > 32), dispatch (histogram,
-    scan, permute, gather; one kernel for the first three up to 4096 pairs over <= 256 experts),
+    scan, permute, gather; one kernel for the first three up to 16384 pairs over <= 256 experts),
     W1/W2, W3, two per shared expert, combine."""
-    small = s.T * s.k <= 4096 and s.E <= 256
+    small = s.T * s.k <= 16384 and s.E <= 256
     return (1 if s.E <= 32 else 2) + (2 if small else 4) + 2 + 2 * s.n_shared + 1
 
 
@@ -230,8 +230,9 @@ def test_empty_batch(moe):
     assert moe.last_launch_count() == 0
 
 
-def test_bad_expert_id_sets_device_error(moe):
-    s = S("bad_ids", T=64, d=64, d_ff=64, E=8, k=2, dtype="bf16", scoring="softmax")
+@pytest.mark.parametrize("T,k,E", [(64, 2, 8), (3000, 8, 64)], ids=["single_block", "chunked"])
+def test_bad_expert_id_sets_device_error(moe, T, k, E):
+    s = S("bad_ids", T=T, d=64, d_ff=64, E=E, k=k, dtype="bf16", scoring="softmax")
     cfg = moe.config_from_shape(s)
     x = torch.randn((s.T, s.d), device="cuda").to(torch.bfloat16)
     idx = torch.arange(s.T * s.k, device="cuda", dtype=torch.int32).reshape(s.T, s.k) % s.E
