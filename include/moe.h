@@ -273,6 +273,17 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
                             const void* Ws3, void* y_host, void* ws, size_t ws_bytes,
                             moe_stream_t stream);
 
+/* moe_forward_host without the final wait: the copy of x_host, the layer and the copy back
+   into y_host are enqueued on `stream` and the call returns.  y_host holds the result once the
+   stream has reached that point (an event or a stream synchronisation), and x_host and y_host
+   must stay valid until then.  With pinned host buffers, calls on two streams (each with its
+   own workspace) overlap one call's copies with the other call's kernels. */
+moe_status moe_forward_host_async(const moe_config* cfg, const void* x_host, const void* W_g,
+                                  const float* logit_bias, const float* sel_bias, const void* W1,
+                                  const void* W2, const void* W3, const void* Ws1, const void* Ws2,
+                                  const void* Ws3, void* y_host, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /* Waits for `stream`, then reads and clears the device error word of the current device.
    Returns MOE_OK, MOE_ERR_DEVICE (and the raw word in *word when word != NULL), or
    MOE_ERR_CUDA when the wait itself failed. */

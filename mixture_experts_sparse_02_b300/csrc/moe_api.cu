@@ -521,10 +521,10 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const void
                       ws_bytes, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(events));
 }
 
-moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const float* logit_bias,
-                            const float* sel_bias, const void* W1, const void* W2, const void* W3, const void* Ws1,
-                            const void* Ws2, const void* Ws3, void* y_host, void* ws, size_t ws_bytes,
-                            moe_stream_t stream) {
+static moe_status forward_host_impl(const moe_config* cfg, const void* x_host, const void* W_g,
+                                    const float* logit_bias, const float* sel_bias, const void* W1, const void* W2,
+                                    const void* W3, const void* Ws1, const void* Ws2, const void* Ws3, void* y_host,
+                                    void* ws, size_t ws_bytes, cudaStream_t st, bool wait) {
   g_launches = 0;
   MOE_TRY(check_config(cfg));
   const moe_config& c = *cfg;
@@ -538,13 +538,32 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
   void* x_dev = w + L.x_io;
   void* y_dev = w + L.y_io;
   const size_t bytes = (size_t)c.T * c.d * esize(c);
-  const cudaStream_t st = (cudaStream_t)stream;
   MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st));
   const moe_status r = forward_impl(cfg, x_dev, W_g, logit_bias, sel_bias, W1, W2, W3, Ws1, Ws2, Ws3, y_dev, nullptr,
                                     nullptr, ws, ws_bytes, st, nullptr);
   if (r != MOE_OK) return r;
   MOE_CUDA(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st));
-  return cuda_status(cudaStreamSynchronize(st));
+  return wait ? cuda_status(cudaStreamSynchronize(st)) : MOE_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const float* logit_bias,
+                            const float* sel_bias, const void* W1, const void* W2, const void* W3, const void* Ws1,
+                            const void* Ws2, const void* Ws3, void* y_host, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  return forward_host_impl(cfg, x_host, W_g, logit_bias, sel_bias, W1, W2, W3, Ws1, Ws2, Ws3, y_host, ws, ws_bytes,
+                           (cudaStream_t)stream, true);
+}
+
+moe_status moe_forward_host_async(const moe_config* cfg, const void* x_host, const void* W_g, const float* logit_bias,
+                                  const float* sel_bias, const void* W1, const void* W2, const void* W3,
+                                  const void* Ws1, const void* Ws2, const void* Ws3, void* y_host, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  return forward_host_impl(cfg, x_host, W_g, logit_bias, sel_bias, W1, W2, W3, Ws1, Ws2, Ws3, y_host, ws, ws_bytes,
+                           (cudaStream_t)stream, false);
 }
 
 moe_status moe_get_device_error(moe_stream_t stream, uint32_t* word) {

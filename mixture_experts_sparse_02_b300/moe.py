@@ -62,6 +62,7 @@ _combine = _sig("moe_combine", [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _
 _forward = _sig("moe_forward", [_CFG] + [_P] * 14 + [_SZ, _P])
 _forward_profiled = _sig("moe_forward_profiled", [_CFG] + [_P] * 14 + [_SZ, _P, _P])
 _forward_host = _sig("moe_forward_host", [_CFG] + [_P] * 12 + [_SZ, _P])
+_forward_host_async = _sig("moe_forward_host_async", [_CFG] + [_P] * 12 + [_SZ, _P])
 _get_device_error = _sig("moe_get_device_error", [_P, ctypes.POINTER(ctypes.c_uint32)])
 _last_launch_count = _sig("moe_last_launch_count", [], ctypes.c_int32)
 _status_string = _sig("moe_status_string", [_I], ctypes.c_char_p)
@@ -74,7 +75,7 @@ _load_stats = _sig("moe_load_stats", [_CFG, _P, _P, _P, _P, ctypes.c_float, _P, 
 DISPATCH_STATIC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = ("moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts", "moe_combine",
-           "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_get_device_error",
+           "moe_forward", "moe_forward_profiled", "moe_forward_host", "moe_forward_host_async", "moe_get_device_error",
            "moe_last_launch_count", "moe_status_string", "moe_dispatch_static", "moe_update_sel_bias",
            "moe_load_stats", "moe_route_expert_choice", "moe_combine_expert_choice", "moe_test_pipeline_fault")
 
@@ -210,6 +211,16 @@ def forward_host(cfg, x_host, W_g, W1, W2, W3, y_host, ws, logit_bias=None, sel_
     _check(_forward_host(ctypes.byref(cfg), _ptr(x_host), _ptr(W_g), _ptr(logit_bias), _ptr(sel_bias), _ptr(W1),
                          _ptr(W2), _ptr(W3), _ptr(Ws1), _ptr(Ws2), _ptr(Ws3), _ptr(y_host), _ptr(ws), nb,
                          _stream(stream)), "moe_forward_host")
+
+
+def forward_host_async(cfg, x_host, W_g, W1, W2, W3, y_host, ws, logit_bias=None, sel_bias=None, Ws1=None, Ws2=None,
+                       Ws3=None, ws_bytes=None, stream=None):
+    """forward_host without the final wait: y_host is ready once `stream` reaches the end of
+    the call (synchronise or record an event)."""
+    nb = ws.numel() * ws.element_size() if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    _check(_forward_host_async(ctypes.byref(cfg), _ptr(x_host), _ptr(W_g), _ptr(logit_bias), _ptr(sel_bias),
+                               _ptr(W1), _ptr(W2), _ptr(W3), _ptr(Ws1), _ptr(Ws2), _ptr(Ws3), _ptr(y_host), _ptr(ws),
+                               nb, _stream(stream)), "moe_forward_host_async")
 
 
 def get_device_error(stream=None) -> int:

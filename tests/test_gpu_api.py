@@ -1,5 +1,6 @@
 """The measurement entry points behave like moe_forward: moe_forward_host (x and y in host
-memory, copies inside the call) and moe_forward_profiled (events at the stage boundaries)."""
+memory, copies inside the call), moe_forward_host_async (the same without the wait, on two
+streams) and moe_forward_profiled (events at the stage boundaries)."""
 import numpy as np
 import pytest
 import torch
@@ -41,6 +42,16 @@ def test_host_and_profiled_match_forward(shape):
     yh = torch.zeros((s.T, s.d), dtype=tdtype(s)).pin_memory()
     moe.forward_host(cfg, xh, Wg, W["W1"], W["W2"], W["W3"], yh, ws, logit_bias=lb, **Ws)
     assert torch.equal(yh, y.cpu())
+    # the asynchronous call on two streams with two workspaces, as a serving loop would
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [ws, torch.empty_like(ws)]
+    ys = [torch.zeros((s.T, s.d), dtype=tdtype(s)).pin_memory() for _ in range(2)]
+    for i in range(4):
+        moe.forward_host_async(cfg, xh, Wg, W["W1"], W["W2"], W["W3"], ys[i % 2], wss[i % 2], logit_bias=lb,
+                               stream=streams[i % 2], **Ws)
+    for st in streams:
+        st.synchronize()
+    assert torch.equal(ys[0], y.cpu()) and torch.equal(ys[1], y.cpu())
     # events at the stage boundaries: same output, the 7 events recorded in order
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_NUM_STAGES + 1)]
     y2 = torch.empty_like(y)
