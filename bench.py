@@ -40,12 +40,13 @@ DEFAULT_WORKLOAD = "mixtral_prefill"
 DECODE_WORKLOAD = "mixtral_decode"
 FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM on the default workload, from
-# one ncu capture of a half-size case scaled to the full launch (profiles/), per kernel
-# variant, valid only for the kernel code it was taken on (gemm_tc.cu without comments; the
-# capture was on the file with sha256 693e133a...).
-NCU_TRAFFIC = {"code_sha256": "5a3daeebef41782d98d3f95a63572c362b426a37418cd1bd0d31af9ae8ae2bc8",
-               "bytes_per_launch": {"pair": 2288.2e6}}
+# DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM, from one ncu capture of a
+# smaller case scaled to the full launch (profiles/), per kernel variant: "pair" for the
+# Mixtral-shaped layer (half the experts and tokens, x 2), "tpairw" for the DeepSeek-V3-shaped
+# one (32 of 256 experts and 1024 of 8192 tokens, x 8).  Valid only for the kernel code it was
+# taken on (gemm_tc.cu without comments; the captures were on the file with sha256 ea4f0c13...).
+NCU_TRAFFIC = {"code_sha256": "c76f10e8a1c94388736e7f6850e2c50885c640a40531675476eb04304a73097e",
+               "bytes_per_launch": {"pair": 2199.7e6, "tpairw": 16704.7e6}}
 
 
 def _code_sha256(path):
@@ -255,12 +256,16 @@ def traffic_for_kernel(variant):
 
 def gemm_variant(shape):
     """Which grouped-GEMM kernel the library runs for the routed W1/W2 + SwiGLU GEMM of this
-    workload: the library's rule (CTA pairs when expert blocks average >= 512 rows, unless
-    MOE_GEMM_KERNEL forces one)."""
+    workload: the library's rule (CTA pairs when expert blocks average >= 512 rows, the
+    token-wide kernel with wide tiles for 128..511, else single CTAs; MOE_GEMM_KERNEL forces
+    one)."""
     forced = os.environ.get("MOE_GEMM_KERNEL")
-    if forced in ("single", "pair", "tpair"):
+    if forced in ("single", "pair", "tpair", "tpairw"):
         return forced
-    return "pair" if shape.T * shape.k >= 512 * shape.E else "single"
+    rows = shape.T * shape.k
+    if rows >= 512 * shape.E:
+        return "pair"
+    return "tpairw" if rows >= 128 * shape.E else "single"
 
 
 def run_ours(args, shape, world, rank, local):
@@ -329,8 +334,8 @@ def run_ours(args, shape, world, rank, local):
     peak = pk["bf16_tflops"]
     ach = fl_w12 / t_w12 / 1e12
     variant = gemm_variant(shape)
-    kname = {"pair": "grouped_gemm_pair_kernel", "tpair": "grouped_gemm_tpair_kernel"}.get(
-        variant, "grouped_gemm_kernel") + "<EPI_SWIGLU>"
+    kname = {"pair": "grouped_gemm_pair_kernel<EPI_SWIGLU>", "tpair": "grouped_gemm_tpair_kernel<EPI_SWIGLU, false>",
+             "tpairw": "grouped_gemm_tpair_kernel<EPI_SWIGLU, true>"}.get(variant, "grouped_gemm_kernel<EPI_SWIGLU>")
     roof = {"bound": "tensor", "kernel": kname + " (W1/W2 + SiLU*mul)",
             "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
             "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(variant),

@@ -72,9 +72,18 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Tile {
   int g, row0, row_end, n_tile;
+  int tile_end;   // end of this tile's rows: row0 + TILE_M, or the group's end for its last tile
 };
 
-template <int TILE_M = BM, typename C>
+// Row tiles of a group of `rows` rows: tiles of TILE_M rows, except that the last one also takes
+// up to WIDE extra rows (so a group of TILE_M + WIDE rows is one tile, not a full tile and a
+// short one).
+template <int TILE_M, int WIDE = 0>
+__host__ __device__ __forceinline__ int row_tiles(int rows) {
+  return rows <= TILE_M + WIDE ? 1 : (rows - WIDE + TILE_M - 1) / TILE_M;
+}
+
+template <int TILE_M = BM, int WIDE = 0, typename C>
 __device__ __forceinline__ Tile decode_tile(const C& c, int G, int t) {
   int lo = 0, hi = G;  // largest g with tile_start[g] <= t (always a non-empty group)
   while (hi - lo > 1) {
@@ -84,18 +93,20 @@ __device__ __forceinline__ Tile decode_tile(const C& c, int G, int t) {
   Tile r;
   r.g = lo;
   const int rows = c.row_off[lo + 1] - c.row_off[lo];
-  const int mt = (rows + TILE_M - 1) / TILE_M;
+  const int mt = row_tiles<TILE_M, WIDE>(rows);
   const int local = t - c.tile_start[lo];
   r.n_tile = local / mt;
-  r.row0 = c.row_off[lo] + (local - r.n_tile * mt) * TILE_M;
+  const int m = local - r.n_tile * mt;
+  r.row0 = c.row_off[lo] + m * TILE_M;
   r.row_end = c.row_off[lo + 1];
+  r.tile_end = m == mt - 1 ? r.row_end : r.row0 + TILE_M;
   return r;
 }
 
 // Warp-wide: the group table of a persistent grouped GEMM.  row_off[g] = offsets[g] clamped
 // to the output's rows (a violation is flagged), tile_start[g] = first tile of group g, with
-// ceil(rows / TILE_M) row tiles times n_tiles column tiles per non-empty group.
-template <int TILE_M, typename C>
+// row_tiles(rows) row tiles times n_tiles column tiles per non-empty group.
+template <int TILE_M, int WIDE = 0, typename C>
 __device__ __forceinline__ void build_group_table(C& c, const GemmArgs& a, int G, int lane) {
   bool bad = false;
   for (int base = 0; base <= G; base += 32) {
@@ -114,7 +125,7 @@ __device__ __forceinline__ void build_group_table(C& c, const GemmArgs& a, int G
     if (g < G) {
       const int rows = c.row_off[g + 1] - c.row_off[g];
       if (rows < 0) bad = true;
-      tiles = rows > 0 ? ((rows + TILE_M - 1) / TILE_M) * a.n_tiles : 0;
+      tiles = rows > 0 ? row_tiles<TILE_M, WIDE>(rows) * a.n_tiles : 0;
     }
     int v = tiles;
 #pragma unroll
@@ -563,25 +574,42 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
 // ------------------------------------------------------------------------- token-wide CTA-pair kernel
 // The CTA-pair GEMM with the operands' roles swapped: the weights' output features run along the
-// MMA's M (256 per pair, 128 per CTA) and the tokens along its N.  N is chosen per tile, in steps
-// of 16 up to 256, so the last tile of an expert's block carries at most 15 rows of padding
-// (with tokens along M the padding reaches 255 rows per expert, about a tenth of the work on
-// the Mixtral-shaped layer).
+// MMA's M (256 per pair, 128 per CTA) and the tokens along its N, in steps of 16, so an expert
+// block pays at most 15 rows of MMA padding (with tokens along M the padding reaches 255 rows per
+// expert, about a tenth of the work on the Mixtral-shaped layer).
+//
+// Tiles hold 256 tokens, except that an expert's last tile also takes up to WIDE = 32 more
+// ("wide" tile): a block of 257..288 rows is one pass over its weight slice instead of a full
+// tile plus a short one.  A short tail tile costs almost as much as a full one, because the
+// weight slice is streamed again for a few tokens; with ~256 rows per expert (DeepSeek-V3
+// shapes) half the experts would need one.  A wide tile issues a second MMA per k step (N = 16
+// or 32) on the same weight stage.
+//
 //   A (MMA M, weights, MN-major): per CTA and stage two 64-feature x 64-k boxes.  SWIGLU: box 0
 //     is W1 for features f0 + 64 r .. + 63 and box 1 is W2 for the same features, so a CTA's
 //     TMEM lanes 0-63 hold X W1 and lanes 64-127 hold X W2 of the same 64 features; EPI_F32:
 //     the two boxes are output features f0 + 128 r .. + 127.
-//   B (MMA N, tokens, K-major): CTA r loads the 128-row box at token row0 + r N / 2; the MMA
-//     takes N / 2 rows from each CTA.
+//   B (MMA N, tokens, K-major): the MMA takes N / 2 rows from each CTA.  A tile of n16 <= 256
+//     (tokens rounded up to 16) has CTA r load the 128-row box at row0 + r n16 / 2.  A wide tile
+//     (n16 = 256 + t16) has CTA r hold rows row0 + r half .. + half - 1, half = 128 + t16 / 2:
+//     a 128-row box (for the N = 256 MMA) and a 16-row box behind it (for the N = t16 MMA).
+//     Accumulator column c of the main MMA is token c (c < 128) or half + c - 128; column c of
+//     the tail MMA is token 128 + c (c < t16 / 2) or half + 128 + c - t16 / 2.
+//   TMEM: two 256-column accumulators (tile i uses buffer i & 1); the tail accumulator of a
+//     wide tile in buffer b borrows columns 0..31 of buffer 1 - b.  The epilogue drains a tile's
+//     tail and its columns 0..31 first and then arrives on thead[b], so the next tile's MMAs
+//     wait only for those two chunks (not the whole drain) before they overwrite them.
 // The SwiGLU epilogue passes X W2 from the warps that hold it (lanes 64-127) to the warps that
 // hold X W1 of the same features through a small shared-memory buffer, 32 tokens at a time.
-// Synchronisation is that of the pair kernel above.
+// Synchronisation is otherwise that of the pair kernel above.
 namespace tpair {
-constexpr int TOK = 256;                           // tokens per pair tile (MMA N)
+constexpr int TOK = 256;                           // tokens of a full tile (MMA N)
+constexpr int WIDE_ROWS = 32;                      // extra tokens an expert's last tile may take
 constexpr int STAGES = 6;
 constexpr int A_BYTES = 2 * B_SUB;                 // 16 KB
-constexpr int B_BYTES = BM * BK * 2;               // 16 KB: 128 token rows x 64 k
-constexpr int STAGE = A_BYTES + B_BYTES;           // 32 KB
+constexpr int B_MAIN = BM * BK * 2;                // 16 KB: 128 token rows x 64 k
+constexpr int B_TAIL_ROWS = WIDE_ROWS / 2;         // 16 rows per CTA for the tail MMA
+constexpr int B_TAIL = B_TAIL_ROWS * BK * 2;       // 2 KB
 constexpr int XCHG_FLOATS = 2 * 32 * 32;           // X W2 of 64 features x 32 tokens
 constexpr uint32_t IDESC_BASE = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(256 >> 4) << 24);
 
@@ -593,6 +621,7 @@ struct Ctrl {
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t thead[2];
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort;
@@ -601,18 +630,115 @@ struct Ctrl {
   int row_off[MAX_GROUPS + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + XCHG_FLOATS * 4 + sizeof(Ctrl);
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// The kernel is compiled with and without wide tiles (W): without, it has no tail MMA, no tail
+// rows in its stages and no early hand-back, and blocks of 257..288 rows take two tiles.
+template <bool W>
+struct Cfg {
+  static constexpr int wide_rows = W ? WIDE_ROWS : 0;
+  static constexpr int STAGE = A_BYTES + B_MAIN + (W ? B_TAIL : 0);   // 34 or 32 KB
+  static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + XCHG_FLOATS * 4 + sizeof(Ctrl);
+  static_assert(STAGE % 1024 == 0, "stage alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Token layout of one tile (see above).
+struct Shape {
+  int n;       // tokens
+  int n16;     // tokens rounded up to 16
+  int t16;     // tail MMA width (0: not a wide tile)
+  int half;    // rows each CTA holds
+  __device__ __forceinline__ Shape(int tokens, bool wide_tiles) {
+    n = tokens;
+    n16 = (tokens + 15) & ~15;
+    t16 = wide_tiles && n16 > TOK ? n16 - TOK : 0;
+    half = t16 ? 128 + t16 / 2 : n16 / 2;
+  }
+  // token of main-accumulator column c (c < 256) or tail-accumulator column c
+  __device__ __forceinline__ int main_token(int c) const { return (t16 == 0 || c < 128) ? c : half + c - 128; }
+  __device__ __forceinline__ int tail_token(int c) const {
+    return c < t16 / 2 ? 128 + c : half + 128 + c - t16 / 2;
+  }
+};
 }  // namespace tpair
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Stores of one 32-column chunk: column j of the chunk is token base + j for j0 <= j < end (the
+// caller splits the chunk into runs on which the token map is affine).  One add, compare and
+// store per column, as few instructions as possible: these warps share issue slots with the
+// TMA producer and the MMA issuer.  SWIGLU: `xv` holds X W2 of the same features.
 template <int EPI>
+__device__ __forceinline__ void tpair_store_run(const GemmArgs& a, const Tile& tl, const uint32_t (&r)[32],
+                                                const float* xv, int lane, int f, int base, int j0, int end) {
+  if (EPI == EPI_SWIGLU) {
+    uint16_t* p = reinterpret_cast<uint16_t*>(a.out) + (size_t)(tl.row0 + base) * a.ldo + f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= j0 && j < end) {
+        const float u = __uint_as_float(r[j]);
+        const float v = xv[j * 32 + lane];
+        const float h = u * __fdividef(v, 1.0f + __expf(-v));
+        p[(size_t)j * a.ldo] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+      }
+    }
+  } else {
+    float* p = reinterpret_cast<float*>(a.out) + (size_t)(tl.row0 + base) * a.ldo + f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= j0 && j < end) {
+        float* dst = p + (size_t)j * a.ldo;
+        const float v = __uint_as_float(r[j]);
+        *dst = a.accumulate ? *dst + v : v;
+      }
+    }
+  }
+}
+
+// Epilogue of 32 accumulator columns of a token-wide tile for this warp's 32 TMEM lanes, already
+// read from TMEM into `r`: store every column whose token is valid.  `tail` selects the
+// column-to-token map: main columns col0 + j are tokens main_token(col0) + j (a chunk never
+// straddles column 128), tail columns j are tokens 128 + j (j < t16 / 2) and half + 128 + j -
+// t16 / 2.  SWIGLU: all four epilogue warps must call it together (named barrier).
+template <int EPI>
+__device__ __forceinline__ void tpair_store_chunk(const GemmArgs& a, const tpair::Shape& sh, const Tile& tl,
+                                                  const uint32_t (&r)[32], int col0, bool tail, int q, int lane,
+                                                  uint32_t rank, float* xchg) {
+  int f;
+  float* xv = nullptr;
+  if (EPI == EPI_SWIGLU) {
+    f = tl.n_tile * 128 + 64 * (int)rank + 32 * (q & 1) + lane;
+    xv = xchg + (q & 1) * 32 * 32;
+    if (q >= 2) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xv[j * 32 + lane] = __uint_as_float(r[j]);
+    }
+    epilogue_bar();
+  } else {
+    f = tl.n_tile * 256 + 128 * (int)rank + 32 * q + lane;
+  }
+  if ((EPI != EPI_SWIGLU || q < 2) && f < a.N) {
+    if (!tail) {
+      const int base = sh.main_token(col0);
+      const int end = min(min(32, (sh.t16 ? tpair::TOK : sh.n16) - col0), sh.n - base);
+      tpair_store_run<EPI>(a, tl, r, xv, lane, f, base, 0, end);
+    } else {
+      const int split = sh.t16 / 2;
+      tpair_store_run<EPI>(a, tl, r, xv, lane, f, 128, 0, min(split, sh.n - 128));
+      const int base_b = sh.half + 128 - split;
+      tpair_store_run<EPI>(a, tl, r, xv, lane, f, base_b, split, min(sh.t16, sh.n - base_b));
+    }
+  }
+  if (EPI == EPI_SWIGLU) epilogue_bar();
+}
+
+template <int EPI, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
-grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
-                          const __grid_constant__ CUtensorMap tmW1, const GemmArgs a) {
+grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXt,
+                          const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                          const GemmArgs a) {
   using tpair::STAGES;
-  using tpair::STAGE;
+  constexpr int STAGE = tpair::Cfg<WIDE>::STAGE;
+  constexpr int WR = tpair::Cfg<WIDE>::wide_rows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -635,19 +761,21 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.tfull[b], 1);
       mbar_init(&c.tempty[b], 8);
+      mbar_init(&c.thead[b], 8);
     }
     mbar_init(&c.drain, 1);
     c.abort = 0;
     fence_barrier_init_cluster();
     fence_proxy_async_smem();
     prefetch_tensormap(&tmX);
+    if (WIDE) prefetch_tensormap(&tmXt);
     prefetch_tensormap(&tmW0);
     prefetch_tensormap(&tmW1);
   }
   if (warp == 2) tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
   pdl_wait();      // offsets, rows and the outputs belong to earlier kernels of the stream
   pdl_trigger();
-  if (warp == 3) build_group_table<tpair::TOK>(c, a, G, lane);
+  if (warp == 3) build_group_table<tpair::TOK, WR>(c, a, G, lane);
   tc_fence_before_sync();
   cluster_sync();
   tc_fence_after_sync();
@@ -662,12 +790,12 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       int s = 0;
       uint32_t phase = 0;
       for (int t = a.starve ? total : cid; t < total; t += nclusters) {
-        const Tile tl = decode_tile<tpair::TOK>(c, G, t);
+        const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
+        const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
         const int z = a.offsets ? tl.g : a.b_z;
-        const int rows = min(tpair::TOK, tl.row_end - tl.row0);
-        const int n_mma = (rows + 15) & ~15;
-        const int trow = tl.row0 + (int)rank * (n_mma >> 1);
+        const int trow = tl.row0 + (int)rank * sh.half;
         const int fa = tl.n_tile * feat_per_tile + (EPI == EPI_SWIGLU ? 64 : 128) * (int)rank;
+        const uint32_t tx = 2u * (uint32_t)(tpair::A_BYTES + tpair::B_MAIN + (sh.t16 ? tpair::B_TAIL : 0));
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&c.empty[s], phase ^ 1, &c.abort, a.wait_limit_ns)) {
@@ -678,7 +806,7 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
           }
           uint8_t* sa = stages + (size_t)s * STAGE;
           uint8_t* sb = sa + tpair::A_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(&c.full[s], 2 * STAGE);
+          if (rank == 0) mbar_arrive_expect_tx(&c.full[s], tx);
           const uint32_t fb = mapa_shared(smem_addr(&c.full[s]), 0);
           const int k0 = kb * BK;
           if (EPI == EPI_SWIGLU) {
@@ -689,6 +817,7 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
             tma_load_3d_pair(sa + B_SUB, &tmW0, fb, fa + 64, k0, z);
           }
           tma_load_2d_pair(sb, &tmX, fb, k0, trow);
+          if (WIDE && sh.t16) tma_load_2d_pair(sb + tpair::B_MAIN, &tmXt, fb, k0, trow + 128);
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -701,33 +830,57 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      bool prev_wide = false;
       for (int t = cid; t < total && ok; t += nclusters, ++it) {
-        const Tile tl = decode_tile<tpair::TOK>(c, G, t);
-        const int rows = min(tpair::TOK, tl.row_end - tl.row0);
-        const uint32_t idesc = tpair::idesc((rows + 15) & ~15);
+        const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
+        const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
+        const bool wide = WIDE && sh.t16 != 0;
+        const uint32_t idesc_main = tpair::idesc(wide ? tpair::TOK : sh.n16);
+        const uint32_t idesc_tail = tpair::idesc(wide ? sh.t16 : 16);
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort, a.wait_limit_ns)) { ok = false; break; }
+        // A wide tile writes columns 0..31 of the other buffer, whose previous tile may still be
+        // draining them; after a wide tile, its tail sits in columns 0..31 of this buffer.
+        if (WIDE && it > 0 && (wide || prev_wide) &&
+            !mbar_wait(&c.thead[buf ^ 1], (uint32_t)((it - 1) >> 1) & 1u, &c.abort, a.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+        const uint32_t d_main = tmem + (uint32_t)(buf * BN);
+        const uint32_t d_tail = tmem + (uint32_t)((buf ^ 1) * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
           const uint32_t sb = sa + tpair::A_BYTES;
+          // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K step
+          // of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.  The
+          // wide test stays outside the K-step loop: a branch between the MMAs of a k-block
+          // slowed the issuing thread measurably.
+          if (wide) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K
-            // step of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.
-            const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
-            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
+              umma_bf16_pair(d_main, ad, sdesc_sw128(sb + kk * 32, 16, 1024), idesc_main, (kb | kk) != 0);
+              umma_bf16_pair(d_tail, ad, sdesc_sw128(sb + tpair::B_MAIN + kk * 32, 16, 1024), idesc_tail,
+                             (kb | kk) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
+              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_bf16_pair(d_main, ad, bd, idesc_main, (kb | kk) != 0);
+            }
           }
           umma_commit_pair(&c.empty[s], 0x3);
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
         if (!ok) break;
         umma_commit_pair(&c.tfull[buf], 0x3);
+        prev_wide = wide;
       }
       if (!ok) {
         flag_error(a.err, ERR_WAIT_MMA);
@@ -742,10 +895,12 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
     const int q = warp & 3;   // TMEM lanes 32 q .. 32 q + 31
     const uint32_t tempty0 = mapa_shared(smem_addr(&c.tempty[0]), 0);
     const uint32_t tempty1 = mapa_shared(smem_addr(&c.tempty[1]), 0);
+    const uint32_t thead0 = mapa_shared(smem_addr(&c.thead[0]), 0);
+    const uint32_t thead1 = mapa_shared(smem_addr(&c.thead[1]), 0);
     int it = 0;
     for (int t = cid; t < total; t += nclusters, ++it) {
-      const Tile tl = decode_tile<tpair::TOK>(c, G, t);
-      const int rows = min(tpair::TOK, tl.row_end - tl.row0);
+      const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
+      const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       // the four epilogue warps take the same decision (they meet at named barriers below)
@@ -760,53 +915,30 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
         break;
       }
       tc_fence_after_sync();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (EPI == EPI_SWIGLU) {
-        // lanes 0-63: X W1, lanes 64-127: X W2, for features fbase .. fbase + 63
-        const int fbase = tl.n_tile * 128 + 64 * (int)rank;
-        const int f = fbase + 32 * (q & 1) + lane;
-        float* xv = xchg + (q & 1) * 32 * 32;
-        uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
-        for (int col0 = 0; col0 < rows; col0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32cols(tbase + col0, r);
-          tmem_ld_wait();
-          if (q >= 2) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) xv[j * 32 + lane] = __uint_as_float(r[j]);
-          }
-          epilogue_bar();
-          if (q < 2 && f < a.N) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < rows) {
-                const float u = __uint_as_float(r[j]);
-                const float v = xv[j * 32 + lane];
-                const float h = u * __fdividef(v, 1.0f + __expf(-v));
-                out[(size_t)(tl.row0 + col0 + j) * a.ldo + f] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-              }
-            }
-          }
-          epilogue_bar();
-        }
-      } else {
-        const int f = tl.n_tile * 256 + 128 * (int)rank + 32 * q + lane;
-        float* out = reinterpret_cast<float*>(a.out);
-        for (int col0 = 0; col0 < rows; col0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32cols(tbase + col0, r);
-          tmem_ld_wait();
-          if (f < a.N) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < rows) {
-                float* dst = out + (size_t)(tl.row0 + col0 + j) * a.ldo + f;
-                const float v = __uint_as_float(r[j]);
-                *dst = a.accumulate ? *dst + v : v;
-              }
-            }
-          }
-        }
+      const uint32_t lanes = (uint32_t)(q * 32) << 16;
+      const uint32_t t_main = tmem + lanes + (uint32_t)(buf * BN);
+      const uint32_t t_tail = tmem + lanes + (uint32_t)((buf ^ 1) * BN);
+      // The tail and columns 0..31 are read first and handed back (thead) before anything is
+      // stored: the next tile's MMAs wait for these two chunks only, and the arrive's release
+      // has no new stores to wait for.
+      if (WIDE) {
+        uint32_t rt[32], rh[32];
+        if (sh.t16) tmem_ld_32cols(t_tail, rt);
+        tmem_ld_32cols(t_main, rh);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? thead1 : thead0);
+        if (sh.t16) tpair_store_chunk<EPI>(a, sh, tl, rt, 0, true, q, lane, rank, xchg);
+        tpair_store_chunk<EPI>(a, sh, tl, rh, 0, false, q, lane, rank, xchg);
+      }
+      const int main_cols = sh.t16 ? tpair::TOK : sh.n16;
+#pragma unroll 1
+      for (int col0 = WIDE ? 32 : 0; col0 < main_cols; col0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(t_main + (uint32_t)col0, r);
+        tmem_ld_wait();
+        tpair_store_chunk<EPI>(a, sh, tl, r, col0, false, q, lane, rank, xchg);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -839,13 +971,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// A operand: rows x K bf16 row-major; box 64 (K) x 128 (rows), 128B swizzle.
-static bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K) {
+// A operand: rows x K bf16 row-major; box 64 (K) x box_rows (rows), 128B swizzle.
+static bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K, int box_rows = BM) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -896,10 +1028,9 @@ struct PairLaunchCache {
   int clusters = 0;
 };
 
-template <typename Kernel>
-static cudaError_t launch_cluster_pair(Kernel kernel, size_t smem, PairLaunchCache& cache, const CUtensorMap& m0,
-                                       const CUtensorMap& m1, const CUtensorMap& m2, const GemmArgs& a,
-                                       cudaStream_t st) {
+template <typename Kernel, typename... Args>
+static cudaError_t launch_cluster_pair(Kernel kernel, size_t smem, PairLaunchCache& cache, cudaStream_t st,
+                                       const Args&... args) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
@@ -928,7 +1059,7 @@ static cudaError_t launch_cluster_pair(Kernel kernel, size_t smem, PairLaunchCac
   }
   cfg.gridDim = dim3(2 * cache.clusters, 1, 1);
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, m2, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
   ++g_launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -937,14 +1068,19 @@ template <int EPI>
 static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
                                const GemmArgs& a, cudaStream_t st) {
   static PairLaunchCache cache;
-  return launch_cluster_pair(grouped_gemm_pair_kernel<EPI>, pair::SMEM_BYTES, cache, ma, mb0, mb1, a, st);
+  return launch_cluster_pair(grouped_gemm_pair_kernel<EPI>, pair::SMEM_BYTES, cache, st, ma, mb0, mb1, a);
 }
 
-template <int EPI>
-static cudaError_t launch_tpair(const CUtensorMap& mx, const CUtensorMap& mw0, const CUtensorMap& mw1,
-                                const GemmArgs& a, cudaStream_t st) {
+// The token-wide kernel with wide tiles also takes the rows through a 16-row box (the tail of a
+// wide tile); without, that map is the main one and is not used.
+template <int EPI, bool WIDE>
+static cudaError_t launch_tpair(const CUtensorMap& mx, const void* A, long long rows_cap, int K,
+                                const CUtensorMap& mw0, const CUtensorMap& mw1, const GemmArgs& a, cudaStream_t st) {
   static PairLaunchCache cache;
-  return launch_cluster_pair(grouped_gemm_tpair_kernel<EPI>, tpair::SMEM_BYTES, cache, mx, mw0, mw1, a, st);
+  CUtensorMap mxt = mx;
+  if (WIDE && !make_map_a(&mxt, A, rows_cap, K, tpair::B_TAIL_ROWS)) return cudaErrorInvalidValue;
+  return launch_cluster_pair(grouped_gemm_tpair_kernel<EPI, WIDE>, tpair::Cfg<WIDE>::SMEM_BYTES, cache, st, mx, mxt,
+                             mw0, mw1, a);
 }
 
 // Test hook: one starved launch with a short wait limit (moe_test_pipeline_fault).
@@ -961,25 +1097,28 @@ static void apply_test_hook(GemmArgs& a) {
 }
 
 // Kernel choice, from measurements on B300 (Mixtral-, Hunyuan- and DeepSeek-V3-shaped layers):
-//   W1/W2 + SwiGLU: the CTA-pair kernel ("pair", 256 token rows per tile) for expert blocks
-//     that average >= 512 rows, else the single-CTA kernel (128-row tiles).  The token-wide pair
-//     kernel is no faster here: its short tail tiles still stream the whole weight slice, and its
-//     epilogue has to pass X W2 between warps.
-//   float32 outputs (W3, router logits): the token-wide CTA-pair kernel ("tpair", tokens along
-//     N in steps of 16) for blocks that average >= 128 rows, else the single-CTA kernel.
-// Decode-sized batches (a few rows per expert) take the single-CTA kernel, which streams each
-// expert's weights once with the fewest bytes per row.  MOE_GEMM_KERNEL=single|pair|tpair
-// overrides the choice (the tests run every kernel on the same inputs).
-enum Variant { V_SINGLE = 0, V_PAIR = 1, V_TPAIR = 2 };
+//   expert blocks averaging >= 512 rows: W1/W2 + SwiGLU on the CTA-pair kernel ("pair", 256
+//     token rows per tile), float32 outputs (W3, router logits) on the token-wide CTA-pair kernel
+//     ("tpair", tokens along N in steps of 16);
+//   128..511 rows (DeepSeek-V3 shapes, ~256 rows per expert): both on the token-wide kernel with
+//     wide tiles ("tpairw"): a block of up to 288 rows is one pass over its weight slice;
+//   fewer rows (decode-sized batches): the single-CTA kernel, which streams each expert's
+//     weights once with the fewest bytes per row.
+// Without wide tiles the token-wide kernel is the faster one on large blocks (its last tile is
+// then a separate short tile, but there is one per four or more full tiles).
+// MOE_GEMM_KERNEL=single|pair|tpair|tpairw overrides the choice (the tests run every kernel on
+// the same inputs).
+enum Variant { V_SINGLE = 0, V_PAIR = 1, V_TPAIR = 2, V_TPAIR_WIDE = 3 };
 
 static Variant choose_variant(int epi, long long rows, int groups) {
   const char* v = getenv("MOE_GEMM_KERNEL");
   if (v && strcmp(v, "single") == 0) return V_SINGLE;
   if (v && strcmp(v, "pair") == 0) return V_PAIR;
   if (v && strcmp(v, "tpair") == 0) return V_TPAIR;
+  if (v && strcmp(v, "tpairw") == 0) return V_TPAIR_WIDE;
   const long long g = groups > 0 ? groups : 1;
-  if (epi == EPI_SWIGLU) return rows >= 512LL * g ? V_PAIR : V_SINGLE;
-  return rows >= 128LL * g ? V_TPAIR : V_SINGLE;
+  if (rows >= 512LL * g) return epi == EPI_SWIGLU ? V_PAIR : V_TPAIR;
+  return rows >= 128LL * g ? V_TPAIR_WIDE : V_SINGLE;
 }
 
 }  // namespace tc
@@ -1001,7 +1140,8 @@ cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, 
   a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
   switch (tc::choose_variant(EPI_SWIGLU, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
-    case tc::V_TPAIR: return tc::launch_tpair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
+    case tc::V_TPAIR: return tc::launch_tpair<EPI_SWIGLU, false>(ma, A, rows_cap, K, mb0, mb1, a, st);
+    case tc::V_TPAIR_WIDE: return tc::launch_tpair<EPI_SWIGLU, true>(ma, A, rows_cap, K, mb0, mb1, a, st);
     case tc::V_PAIR: return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
     default: return tc::launch<EPI_SWIGLU>(ma, mb0, mb1, a, st);
   }
@@ -1019,7 +1159,8 @@ cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* 
   a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
   switch (tc::choose_variant(EPI_F32, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
-    case tc::V_TPAIR: return tc::launch_tpair<EPI_F32>(ma, mb, mb, a, st);
+    case tc::V_TPAIR: return tc::launch_tpair<EPI_F32, false>(ma, A, rows_cap, K, mb, mb, a, st);
+    case tc::V_TPAIR_WIDE: return tc::launch_tpair<EPI_F32, true>(ma, A, rows_cap, K, mb, mb, a, st);
     case tc::V_PAIR: return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
     default: return tc::launch<EPI_F32>(ma, mb, mb, a, st);
   }

@@ -18,7 +18,7 @@ ERR_WAIT_MMA = 1 << 3
 ERR_WAIT_EPILOGUE = 1 << 4
 
 
-@pytest.mark.parametrize("variant", ["single", "pair", "tpair"])
+@pytest.mark.parametrize("variant", ["single", "pair", "tpair", "tpairw"])
 def test_starved_pipeline_times_out_and_reports(variant, monkeypatch):
     moe = require_cuda()
     monkeypatch.setenv("MOE_GEMM_KERNEL", variant)

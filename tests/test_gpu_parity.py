@@ -47,7 +47,16 @@ GEMM_SHAPES = [
     S("gemm_skewed_e64", T=257, d=256, d_ff=320, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.5),
     S("gemm_two_shared", T=300, d=384, d_ff=200, E=40, k=1, dtype="bf16", scoring="sigmoid",
       n_shared=2, d_ff_shared=72),
+    # 280 rows per shared expert: one wide token tile, accumulated by the second shared expert
+    S("gemm_wide_shared", T=280, d=256, d_ff=200, E=8, k=2, dtype="bf16", scoring="softmax",
+      n_shared=2, d_ff_shared=72),
 ]
+
+# Expert block sizes on every boundary of the kernels' row tiles: empty; around the 16-row
+# steps of the token-wide tiles; 128 and 256 +- 1; one wide token tile (257..288: a full tile
+# plus up to 32 rows); a full tile and a short one (289, 300); a full and a wide tile (544);
+# three tiles (545).
+TILE_BOUNDARY_COUNTS = [0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 272, 273, 288, 289, 300, 544, 545, 31]
 
 
 @pytest.fixture(scope="module")
@@ -145,7 +154,7 @@ def test_stages_small(moe, shape):
     assert moe.get_device_error() == 0
 
 
-@pytest.mark.parametrize("variant", ["single", "pair", "tpair"])
+@pytest.mark.parametrize("variant", ["single", "pair", "tpair", "tpairw"])
 @pytest.mark.parametrize("shape", GEMM_SHAPES, ids=[s.name for s in GEMM_SHAPES])
 def test_gemm_kernels(moe, shape, variant, monkeypatch):
     """Each grouped-GEMM kernel, forced, against the oracle: the experts call alone (oracle
@@ -169,6 +178,28 @@ def test_gemm_kernels(moe, shape, variant, monkeypatch):
     y, idx, _ = _forward(moe, case, W, _device_inputs(case))
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
     assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+
+
+@pytest.mark.parametrize("variant", ["single", "pair", "tpair", "tpairw"])
+def test_gemm_tile_boundaries(moe, variant, monkeypatch):
+    """The experts call on rows already grouped by expert, with block sizes on every tile
+    boundary, against the oracle's grouped evaluation (every output row compared)."""
+    monkeypatch.setenv("MOE_GEMM_KERNEL", variant)
+    counts = np.array(TILE_BOUNDARY_COUNTS, dtype=np.int64)
+    s = S("gemm_tile_boundaries", T=int(counts.sum()), d=384, d_ff=320, E=len(counts), k=1, dtype="bf16",
+          scoring="softmax")
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = wl.gen_x(s, 0)                      # the rows of x_perm, in expert order
+    W = upload_experts(s, 0, keep=range(s.E))
+    ref = orc.experts_grouped(wl.to_f64(x, s.dtype), offsets, host_weight_fn(W["host"], s))
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    y_perm = torch.full((s.T, s.d), float("nan"), dtype=torch.float32, device="cuda")
+    moe.experts(cfg, to_dev(x, s), torch.from_numpy(offsets).cuda(), W["W1"], W["W2"], W["W3"], y_perm, ws)
+    assert moe.get_device_error() == 0
+    got = dev_to_f64(y_perm)
+    assert np.isfinite(got).all()           # every row written
+    assert max_rel_err(got, ref) <= y_tol(s)
 
 
 FULL = ["mixtral_prefill", "mixtral_decode", "hunyuan_a13b", "deepseek_v3"]
