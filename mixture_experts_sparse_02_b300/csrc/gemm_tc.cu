@@ -12,7 +12,7 @@
 // Three kernels, all persistent (one CTA per SM, or one CTA pair per two SMs), all reading the
 // group sizes on the device from `offsets` (nothing is synchronised with the host):
 //   grouped_gemm_kernel        1 CTA, 128 token rows x 256 MMA columns per tile, 4 x 48 KB
-//                              stages.  For small expert blocks (decode) and ragged ones.
+//                              stages.  For small expert blocks (decode, < 128 rows).
 //   grouped_gemm_pair_kernel   a cluster of 2 CTAs shares one tcgen05.mma.cta_group::2 of
 //                              256 token rows x 256 columns; each CTA loads its 128 rows and
 //                              half of the weight columns; 6 x 32 KB stages.  W1/W2 + SwiGLU
@@ -20,7 +20,9 @@
 //   grouped_gemm_tpair_kernel  the CTA pair with the roles swapped: weight features along the
 //                              MMA's M (256), tokens along N in steps of 16 up to 256, so the
 //                              last tile of a block carries at most 15 padding rows.  The
-//                              float32-output GEMMs for blocks averaging >= 128 rows.
+//                              float32-output GEMMs for blocks averaging >= 512 rows; with
+//                              "wide" tiles (an expert's last tile takes up to 32 more tokens)
+//                              both GEMMs for blocks averaging 128..511 rows.
 // Tiles are walked as (group, column tile, row tile), row tiles fastest, so the CTAs that run
 // at the same time share one weight tile and the weights are streamed from HBM about once.
 // Row tiles may run past the end of their group: the extra rows belong to the next group (or
