@@ -38,10 +38,11 @@ SMALL = [
     S("f32_e2", T=90, d=64, d_ff=32, E=2, k=1, dtype="f32", scoring="sigmoid"),
 ]
 
-# Shapes for running every grouped-GEMM kernel (128-row single-CTA tiles, 256-row CTA-pair
-# tiles, token-wide CTA-pair tiles of 16..256 tokens) on the same inputs: ragged groups that end
-# inside a tile, empty experts, a group larger than one pair tile, N not a multiple of the tile
-# width, shared experts accumulating.
+# Shapes for running every grouped-GEMM kernel on the same inputs: 128-row single-CTA tiles,
+# 256-row CTA-pair tiles, and token-wide CTA-pair tiles of 16..256 tokens, with and without
+# wide last tiles of up to 288 tokens.  They cover ragged groups that end inside a tile, empty
+# experts, a group larger than one pair tile, N not a multiple of the tile width, and shared
+# experts accumulating.
 GEMM_SHAPES = [
     S("gemm_ragged_e6", T=1000, d=512, d_ff=776, E=6, k=2, dtype="bf16", scoring="softmax", logit_bias_std=1.0),
     S("gemm_skewed_e64", T=257, d=256, d_ff=320, E=64, k=8, dtype="bf16", scoring="softmax", logit_bias_std=1.5),
