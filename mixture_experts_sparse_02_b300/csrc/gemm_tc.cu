@@ -833,6 +833,8 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       int it = 0;
       bool ok = true;
       bool prev_wide = false;
+      const uint64_t ad_base = sdesc_sw128(smem_addr(stages), B_SUB, 1024);
+      const uint64_t bd_base = sdesc_sw128(smem_addr(stages) + tpair::A_BYTES, 16, 1024);
       for (int t = cid; t < total && ok; t += nclusters, ++it) {
         const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
         const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
@@ -855,27 +857,26 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
-          const uint32_t sb = sa + tpair::A_BYTES;
           // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K step
           // of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.  The
-          // wide test stays outside the K-step loop: a branch between the MMAs of a k-block
-          // slowed the issuing thread measurably.
+          // descriptors are the stage-0 ones plus the byte offset / 16 in their address field
+          // (shared addresses stay below 2^18, so the field never carries), and the wide test
+          // stays outside the K-step loop: the issuing thread is on the critical path.
+          const uint64_t soff = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
+          const uint64_t ad0 = ad_base + soff, bd0 = bd_base + soff;
           if (wide) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
-              umma_bf16_pair(d_main, ad, sdesc_sw128(sb + kk * 32, 16, 1024), idesc_main, (kb | kk) != 0);
-              umma_bf16_pair(d_tail, ad, sdesc_sw128(sb + tpair::B_MAIN + kk * 32, 16, 1024), idesc_tail,
-                             (kb | kk) != 0);
+              const uint64_t ad = ad0 + (uint64_t)(kk * (2048 >> 4));
+              const uint64_t bd = bd0 + (uint64_t)(kk * (32 >> 4));
+              umma_bf16_pair(d_main, ad, bd, idesc_main, (kb | kk) != 0);
+              umma_bf16_pair(d_tail, ad, bd + (uint64_t)(tpair::B_MAIN >> 4), idesc_tail, (kb | kk) != 0);
             }
           } else {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(sa + kk * 2048, B_SUB, 1024);
-              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-              umma_bf16_pair(d_main, ad, bd, idesc_main, (kb | kk) != 0);
-            }
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_pair(d_main, ad0 + (uint64_t)(kk * (2048 >> 4)), bd0 + (uint64_t)(kk * (32 >> 4)), idesc_main,
+                             (kb | kk) != 0);
           }
           umma_commit_pair(&c.empty[s], 0x3);
           if (++s == STAGES) { s = 0; phase ^= 1; }
