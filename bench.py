@@ -44,9 +44,9 @@ FLUSH_BYTES = 256 << 20
 # smaller case scaled to the full launch (profiles/), per kernel variant: "pair" for the
 # Mixtral-shaped layer (half the experts and tokens, x 2), "tpairw" for the DeepSeek-V3-shaped
 # one (32 of 256 experts and 1024 of 8192 tokens, x 8).  Valid only for the kernel code it was
-# taken on (gemm_tc.cu without comments; the captures were on the file with sha256 ea4f0c13...).
-NCU_TRAFFIC = {"code_sha256": "c76f10e8a1c94388736e7f6850e2c50885c640a40531675476eb04304a73097e",
-               "bytes_per_launch": {"pair": 2199.7e6, "tpairw": 16704.7e6}}
+# taken on (gemm_tc.cu without comments; the captures were on the file with sha256 d91cdabb...).
+NCU_TRAFFIC = {"code_sha256": "8d9d90722e723748df0868624429007cb3e672eb7ff4fec1cfd3277912643e93",
+               "bytes_per_launch": {"pair": 2211.0e6, "tpairw": 16718.2e6}}
 
 
 def _code_sha256(path):

@@ -298,6 +298,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      // Stage-0 descriptors; a stage or K step adds its byte offset / 16 to the address field
+      // (shared addresses stay below 2^18, so the field never carries).
+      const uint64_t ad_base = sdesc_sw128(smem_addr(stages), 16, 1024);
+      const uint64_t bd_base = sdesc_sw128(smem_addr(stages) + A_TILE, B_SUB, 1024);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
@@ -307,16 +311,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
-          const uint32_t sb = sa + A_TILE;
+          const uint64_t soff = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A: K-major rows of 128 B; a K step of 16 elements moves 32 B inside the swizzle atom.
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
             // B: MN-major; 8-row k-groups 1024 B apart, 64-column n-blocks B_SUB apart;
             // a K step of 16 rows moves 2048 B.
-            const uint64_t bd = sdesc_sw128(sb + kk * 2048, B_SUB, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            umma_bf16(d_tmem, ad_base + soff + (uint64_t)(kk * (32 >> 4)), bd_base + soff + (uint64_t)(kk * (2048 >> 4)),
+                      IDESC, (kb | kk) != 0);
           }
           umma_commit(&c.empty[s]);
           if (++s == STAGES) { s = 0; phase ^= 1; }
@@ -504,6 +506,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      const uint64_t ad_base = sdesc_sw128(smem_addr(stages), 16, 1024);   // stage 0, as above
+      const uint64_t bd_base = sdesc_sw128(smem_addr(stages) + pair::A_TILE, B_SUB, 1024);
       for (int t = cid; t < total && ok; t += nclusters, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
@@ -513,15 +517,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after_sync();
-          const uint32_t sa = smem_addr(stages + (size_t)s * STAGE);
-          const uint32_t sb = sa + pair::A_TILE;
+          const uint64_t soff = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // Same layouts as the single-CTA kernel; each CTA supplies its 128 rows of A and
             // its two 64-column blocks of B at these shared-memory offsets.
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + kk * 2048, B_SUB, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, pair::IDESC, (kb | kk) != 0);
+            umma_bf16_pair(d_tmem, ad_base + soff + (uint64_t)(kk * (32 >> 4)),
+                           bd_base + soff + (uint64_t)(kk * (2048 >> 4)), pair::IDESC, (kb | kk) != 0);
           }
           umma_commit_pair(&c.empty[s], 0x3);
           if (++s == STAGES) { s = 0; phase ^= 1; }
