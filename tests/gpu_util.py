@@ -12,7 +12,7 @@ import workloads as wl
 
 BF16_TOL = 2e-2    # max|err| <= 2e-2 * rms(ref) for bfloat16 weights and activations
 F32_TOL = 1e-4     # max|err| <= 1e-4 * rms(ref) for the float32 layer
-GATE_ATOL = 1e-5   # gates: float32 from float32 logits (tolerances)
+GATE_ATOL = 1e-5   # gates: computed in float32 on the GPU from the same float32 logits as the oracle
 
 
 def require_cuda():
