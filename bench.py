@@ -12,9 +12,11 @@ so tokens shard with no exchange): weak scaling, no collective on the data path.
 Rank 0 prints one JSON line.  `value` = tokens of all ranks / max-over-ranks device time.
 `e2e` is the same through moe_forward_host_async with x and y in pinned host memory (two
 streams, so that one step's host copies overlap another step's kernels); `e2e.sync` is the
-synchronous moe_forward_host, step after step.  `roofline`
-is the W1/W2 + SwiGLU grouped GEMM (the dominant kernel).  `cpu_baseline` is the CPU oracle
-on a bounded sample on this host.  `--impl reference` times that oracle alone.
+synchronous moe_forward_host, step after step.  `roofline` is the W1/W2 + SwiGLU grouped GEMM
+(the dominant kernel).  `cpu_baseline` is the CPU oracle on a bounded sample on this host.
+At N = 1 the line also carries `workloads`: the same record (tokens/s, stage times, expert-GEMM
+fraction of the bf16 peak, roofline, e2e, its own CPU-oracle sample) for the Hunyuan-A13B-shaped,
+DeepSeek-V3-shaped and float32 workloads.  `--impl reference` times the oracle alone.
 """
 from __future__ import annotations
 
@@ -38,15 +40,21 @@ import workloads as wl  # noqa: E402
 METRIC = "MoE-layer tokens/sec on 1 B300; expert-GEMM % of bf16 peak; decode HBM GB/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
 DECODE_WORKLOAD = "mixtral_decode"
+# measured after the headline workload in the default run (N = 1): the Hunyuan-A13B-shaped and
+# DeepSeek-V3-shaped prefill layers and the float32 correctness layer
+EXTRA_WORKLOADS = ("hunyuan_a13b", "deepseek_v3", "tiny_f32")
+# tokens per CPU-oracle sample, sized for a few seconds of host time per workload
+ORACLE_SAMPLE_TOKENS = {"tiny_f32": 64, "mixtral_prefill": 64, "mixtral_decode": 16, "hunyuan_a13b": 32,
+                        "deepseek_v3": 8}
 FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) per launch of the W1/W2 SwiGLU GEMM, from one ncu capture of a
-# smaller case scaled to the full launch (profiles/), per kernel variant: "pair" for the
-# Mixtral-shaped layer (half the experts and tokens, x 2), "tpairw" for the DeepSeek-V3-shaped
-# one (32 of 256 experts and 1024 of 8192 tokens, x 8).  Valid only for the kernel code it was
-# taken on (gemm_tc.cu without comments; the captures were on the file with sha256 d91cdabb...).
+# DRAM bytes (read + write) per launch of each workload's W1/W2 SwiGLU GEMM, from one ncu
+# capture of a smaller case scaled to the full launch (profiles/): the Mixtral-shaped layer
+# (half the experts and tokens, x 2) and the DeepSeek-V3-shaped one (32 of 256 experts and
+# 1024 of 8192 tokens, x 8).  Valid only for the kernel code it was taken on (gemm_tc.cu
+# without comments, by sha256); null otherwise.
 NCU_TRAFFIC = {"code_sha256": "8d9d90722e723748df0868624429007cb3e672eb7ff4fec1cfd3277912643e93",
-               "bytes_per_launch": {"pair": 2211.0e6, "tpairw": 16718.2e6}}
+               "bytes_per_launch": {"mixtral_prefill": 2211.0e6, "deepseek_v3": 16718.2e6}}
 
 
 def _code_sha256(path):
@@ -157,29 +165,29 @@ def barrier(world):
         dist.barrier()
 
 
-# ----------------------------------------------------------------------------- CPU oracle legs
+# ----------------------------------------------------------------------------- host and CPU oracle legs
 
-def oracle_sample_step(shape, host, n_tokens: int, seed: int = 0) -> float:
-    """The CPU oracle, as it stands, on the first n_tokens tokens of the workload.  Returns the
-    wall seconds (input generation excluded)."""
-    from oracle import moe_oracle as orc
-    x64 = wl.to_f64(host["x"][:n_tokens], shape.dtype)
-    Wg = wl.to_f64(host["W_g"], shape.dtype)
-    get_w = orc.weights_from_arrays(host["weights"], shape.dtype)
-    t0 = time.perf_counter()
-    orc.forward(x64, Wg, get_w, shape.E, shape.k, shape.scoring, host.get("logit_bias"), None, shape.n_shared)
-    return time.perf_counter() - t0
-
-
-def host_inputs(shape, seed=0, x_seed=None):
-    w = {}
-    for name in ("W1", "W2", "W3") + (("Ws1", "Ws2", "Ws3") if shape.n_shared else ()):
-        w[name] = wl.gen_experts(shape, name, seed)
-    return {"x": wl.gen_x(shape, seed if x_seed is None else x_seed), "W_g": wl.gen_router(shape, seed),
-            "logit_bias": wl.gen_logit_bias(shape, seed), "weights": w}
+def host_cpu():
+    """(CPU model name, CPUs this process may run on)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        n = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        n = os.cpu_count() or 1
+    return model, n
 
 
 def cpu_threads() -> int:
+    """Threads of numpy's BLAS pool: the most threads the oracle runs at once (its matrix
+    products; the rest of it is single-threaded numpy)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") in ("openblas", "mkl")]
@@ -190,24 +198,81 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_experts_needed(shape, x_rows, W_g, logit_bias):
+    """Experts that the oracle's routing of these token rows picks: only their weights need a
+    host copy for the CPU-oracle sample."""
+    from oracle import moe_oracle as orc
+    r = orc.route(wl.to_f64(x_rows, shape.dtype), wl.to_f64(W_g, shape.dtype), shape.k, shape.scoring, logit_bias)
+    # the grouped evaluation also reads expert 0's W3 for the output width
+    return sorted(set(int(e) for e in np.unique(r["idx"])) | {0})
+
+
+def oracle_sample(shape, x_rows, W_g, logit_bias, get_w) -> float:
+    """The CPU oracle, as it stands, on the given token rows: router, dispatch, one float64
+    SwiGLU per expert block, combine (+ shared experts).  Returns the wall seconds (the inputs
+    are drawn beforehand and not timed)."""
+    from oracle import moe_oracle as orc
+    x64 = wl.to_f64(x_rows, shape.dtype)
+    Wg = wl.to_f64(W_g, shape.dtype)
+    t0 = time.perf_counter()
+    orc.forward(x64, Wg, get_w, shape.E, shape.k, shape.scoring, logit_bias, None, shape.n_shared)
+    return time.perf_counter() - t0
+
+
+def sample_tokens(args, shape) -> int:
+    n = args.ref_tokens if args.ref_tokens else ORACLE_SAMPLE_TOKENS.get(shape.name, 16)
+    return max(1, min(shape.T, n))
+
+
+def cpu_record(shape, seconds, n_tok, per="one pass") -> dict:
+    model, ncpu = host_cpu()
+    return {"value": n_tok / seconds, "unit": "tokens/s", "cores": cpu_threads(), "host_cpus": ncpu,
+            "cpu_model": model, "kind": "oracle", "seconds": round(seconds, 3),
+            "sample": "first %d of the workload's %d tokens, %s (fp32 router, fp64 experts and combine; "
+                      "a correctness oracle, not a tuned CPU MoE)" % (n_tok, shape.T, per)}
+
+
+def host_weights(shape, experts, seed=0):
+    """Host copies (stored dtype) of the routed experts in `experts` and of every shared expert,
+    drawn in parallel."""
+    from concurrent.futures import ThreadPoolExecutor
+    jobs = [(name, e) for name in ("W1", "W2", "W3") for e in experts]
+    jobs += [(name, s) for name in (("Ws1", "Ws2", "Ws3") if shape.n_shared else ()) for s in range(shape.n_shared)]
+    _, ncpu = host_cpu()
+    with ThreadPoolExecutor(max(4, min(32, ncpu))) as ex:
+        arrays = list(ex.map(lambda j: wl.gen_expert(shape, j[0], j[1], seed), jobs))
+    return dict(zip(jobs, arrays))
+
+
+def workload_config(shape, world) -> dict:
+    return {"workload": shape.name, "T": shape.T, "d": shape.d, "d_ff": shape.d_ff, "E": shape.E, "k": shape.k,
+            "scoring": shape.scoring, "n_shared": shape.n_shared, "d_ff_shared": shape.d_ff_shared,
+            "logit_bias_std": shape.logit_bias_std, "tokens_per_gpu": shape.T,
+            "parallelism": "replicas (token shards)" if world > 1 else "1 GPU",
+            "l2": "flushed between steps (256 MiB write)"}
+
+
 def run_reference(args, shape, world, rank):
     if rank != 0:
         return 0
-    host = host_inputs(shape)
-    n_tok = args.ref_tokens
+    n_tok = sample_tokens(args, shape)
+    x = wl.gen_x(shape, 0)[:n_tok]
+    W_g = wl.gen_router(shape, 0)
+    lb = wl.gen_logit_bias(shape, 0)
+    host = host_weights(shape, oracle_experts_needed(shape, x, W_g, lb))
+    get_w = lambda name, e: wl.to_f64(host[(name, e)], shape.dtype)
     for _ in range(args.warmup):
-        oracle_sample_step(shape, host, n_tok)
-    times = [oracle_sample_step(shape, host, n_tok) for _ in range(args.steps)]
+        oracle_sample(shape, x, W_g, lb, get_w)
+    times = [oracle_sample(shape, x, W_g, lb, get_w) for _ in range(args.steps)]
     total = sum(times)
     value = n_tok * args.steps / total
+    cpu = cpu_record(shape, total / args.steps, n_tok, "per step")
+    cpu["value"] = value
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded generator)",
-            "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "d_ff": shape.d_ff, "E": shape.E,
-                       "k": shape.k, "sampled_tokens_per_step": n_tok},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                             "sample": "first %d tokens of the workload per step (fp32 router, fp64 experts)" % n_tok},
+            "data": "synthetic (seeded generator)", "config": workload_config(shape, world),
+            "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -215,7 +280,9 @@ def run_reference(args, shape, world, rank):
 
 # ----------------------------------------------------------------------------- GPU leg
 
-def upload_weights(shape, torch, seed=0):
+def upload_weights(shape, torch, seed=0, keep=()):
+    """Draw every expert matrix (in parallel), copy it to the device, and keep host copies of
+    the routed experts in `keep` and, when `keep` is not None, of the shared experts."""
     from concurrent.futures import ThreadPoolExecutor
     dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
     W = {}
@@ -225,19 +292,22 @@ def upload_weights(shape, torch, seed=0):
         rows, cols, _ = wl.expert_dims(shape, name)
         W[name] = torch.empty((n, rows, cols), dtype=dt, device="cuda")
         jobs += [(name, e) for e in range(n)]
-    host = {name: [None] * W[name].shape[0] for name in W}
+    keep_set = None if keep is None else set(int(e) for e in keep)
+    host = {}
 
     def one(job):
         name, e = job
         a = wl.gen_expert(shape, name, e, seed)
-        host[name][e] = a
+        if keep_set is not None and (name.startswith("Ws") or e in keep_set):
+            host[(name, e)] = a
         t = torch.from_numpy(a)
         W[name][e].copy_(t.view(dt) if shape.dtype == "bf16" else t)
 
-    with ThreadPoolExecutor(16) as ex:
+    _, ncpu = host_cpu()
+    with ThreadPoolExecutor(max(4, min(32, ncpu))) as ex:
         list(ex.map(one, jobs))
     torch.cuda.synchronize()
-    return W, {k: np.stack(v) for k, v in host.items()}
+    return W, host
 
 
 def to_dev(torch, a, shape):
@@ -247,18 +317,20 @@ def to_dev(torch, a, shape):
     return t.cuda()
 
 
-def traffic_for_kernel(variant):
+def traffic_for(workload):
     src = os.path.join(ROOT, "mixture_experts_sparse_02_b300", "csrc", "gemm_tc.cu")
     if NCU_TRAFFIC["code_sha256"] and os.path.exists(src) and _code_sha256(src) == NCU_TRAFFIC["code_sha256"]:
-        return NCU_TRAFFIC["bytes_per_launch"].get(variant)
+        return NCU_TRAFFIC["bytes_per_launch"].get(workload)
     return None
 
 
 def gemm_variant(shape):
     """Which grouped-GEMM kernel the library runs for the routed W1/W2 + SwiGLU GEMM of this
     workload: the library's rule (CTA pairs when expert blocks average >= 512 rows, the
-    token-wide kernel with wide tiles for 128..511, else single CTAs; MOE_GEMM_KERNEL forces
-    one)."""
+    token-wide kernel with wide tiles for 128..511, else single CTAs; f32 layers run on CUDA
+    cores; MOE_GEMM_KERNEL forces one)."""
+    if shape.dtype != "bf16":
+        return "simt"
     forced = os.environ.get("MOE_GEMM_KERNEL")
     if forced in ("single", "pair", "tpair", "tpairw"):
         return forced
@@ -268,28 +340,38 @@ def gemm_variant(shape):
     return "tpairw" if rows >= 128 * shape.E else "single"
 
 
-def run_ours(args, shape, world, rank, local):
+KERNEL_NAMES = {"pair": "grouped_gemm_pair_kernel<EPI_SWIGLU>",
+                "tpair": "grouped_gemm_tpair_kernel<EPI_SWIGLU, false>",
+                "tpairw": "grouped_gemm_tpair_kernel<EPI_SWIGLU, true>",
+                "single": "grouped_gemm_kernel<EPI_SWIGLU>",
+                "simt": "simt_swiglu_f32 (CUDA cores, float32)"}
+
+
+def measure_workload(args, shape, world, rank, pk, headline):
+    """One workload on this rank's GPU: W warm-up steps, K timed steps of moe_forward_profiled
+    (L2 flushed before each), the per-stage split, the end-to-end host-buffer runs and the
+    CPU-oracle sample.  Returns the record (the headline JSON line's fields)."""
     import torch
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from mixture_experts_sparse_02_b300 import moe
 
-    pk = peaks()
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    n_tok = sample_tokens(args, shape)
     # replicated weights (seed 0); each rank draws its own tokens
-    W, W_host = upload_weights(shape, torch, 0)
     x_host = wl.gen_x(shape, 0 if rank == 0 else 1000 + rank)
-    x = to_dev(torch, x_host, shape)
-    W_g = to_dev(torch, wl.gen_router(shape, 0), shape)
+    Wg_host = wl.gen_router(shape, 0)
     lb_np = wl.gen_logit_bias(shape, 0)
+    keep = oracle_experts_needed(shape, x_host[:n_tok], Wg_host, lb_np) if want_cpu else None
+    t_gen = time.perf_counter()
+    W, W_host = upload_weights(shape, torch, 0, keep)
+    gen_s = time.perf_counter() - t_gen
+    x = to_dev(torch, x_host, shape)
+    W_g = to_dev(torch, Wg_host, shape)
     lb = None if lb_np is None else torch.from_numpy(lb_np).cuda()
     cfg = moe.config_from_shape(shape)
     ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
     dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
     y = torch.empty((shape.T, shape.d), dtype=dt, device="cuda")
     flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
     Ws = dict(Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"))
 
     def step(events=None):
@@ -300,7 +382,7 @@ def run_ours(args, shape, world, rank, local):
         step()
     torch.cuda.synchronize()
     if moe.get_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
+        raise RuntimeError("device error word set during warm-up (%s)" % shape.name)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_NUM_STAGES + 1)] for _ in range(args.steps)]
     launches = 0
@@ -318,35 +400,36 @@ def run_ours(args, shape, world, rank, local):
                 for i in range(args.steps)]
     total_s = sum(step_ms) / 1e3
     total_s_max = max_over_ranks(total_s, world, device="cuda")
-    tokens = shape.T * args.steps * world
-    value = tokens / total_s_max
+    value = shape.T * args.steps * world / total_s_max
     mean_stage = [statistics.mean(s[j] for s in stage_ms) for j in range(moe.MOE_NUM_STAGES)]
     stages = dict(zip(moe.STAGE_NAMES, [round(v, 4) for v in mean_stage]))
 
-    # algorithmic work
+    # algorithmic work: W1/W2 + SwiGLU 4 d d_ff per routed row, W3 2 d d_ff, shared 6 d d_ffs per token
     N = shape.T * shape.k
     fl_w12 = 4.0 * N * shape.d * shape.d_ff
     fl_w3 = 2.0 * N * shape.d * shape.d_ff
     fl_sh = 6.0 * shape.T * shape.d * shape.d_ff_shared * shape.n_shared
-    t_w12 = mean_stage[2] / 1e3
-    t_w3 = mean_stage[3] / 1e3
-    t_sh = mean_stage[4] / 1e3
+    t_w12, t_w3, t_sh = mean_stage[2] / 1e3, mean_stage[3] / 1e3, mean_stage[4] / 1e3
     peak = pk["bf16_tflops"]
     ach = fl_w12 / t_w12 / 1e12
+    expert_tflops = (fl_w12 + fl_w3 + fl_sh) / (t_w12 + t_w3 + t_sh) / 1e12
     variant = gemm_variant(shape)
-    kname = {"pair": "grouped_gemm_pair_kernel<EPI_SWIGLU>", "tpair": "grouped_gemm_tpair_kernel<EPI_SWIGLU, false>",
-             "tpairw": "grouped_gemm_tpair_kernel<EPI_SWIGLU, true>"}.get(variant, "grouped_gemm_kernel<EPI_SWIGLU>")
-    roof = {"bound": "tensor", "kernel": kname + " (W1/W2 + SiLU*mul)",
-            "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-            "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for_kernel(variant),
-            "traffic_unit": "bytes per launch (dram read + write)",
-            "algorithmic_flops_per_launch": fl_w12}
-    eg_t = t_w12 + t_w3 + t_sh
-    expert_tflops = (fl_w12 + fl_w3 + fl_sh) / eg_t / 1e12
+    if shape.dtype == "bf16":
+        roof = {"bound": "tensor", "kernel": KERNEL_NAMES[variant] + " (W1/W2 + SiLU*mul)",
+                "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for(shape.name),
+                "traffic_unit": "bytes per launch (dram read + write)", "algorithmic_flops_per_launch": fl_w12}
+        eg = {"tflops": round(expert_tflops, 2), "frac_of_peak": round(expert_tflops / peak, 4), "peak_tflops": peak,
+              "w12_ms": round(mean_stage[2], 4), "w3_ms": round(mean_stage[3], 4), "shared_ms": round(mean_stage[4], 4)}
+    else:
+        roof = {"bound": "latency", "kernel": KERNEL_NAMES[variant], "achieved": round(ach, 4), "peak": None,
+                "unit": "TFLOP/s", "frac": None, "traffic": None,
+                "note": "float32 correctness workload: a few microseconds per kernel, bound by launch latency"}
+        eg = {"tflops": round(expert_tflops, 4), "frac_of_peak": None}
 
     # decode-shaped batch with the same weights (T = 16 tokens): touched-expert weight bytes / time
     decode = None
-    if shape.name == DEFAULT_WORKLOAD and not args.no_decode:
+    if headline and shape.name == DEFAULT_WORKLOAD and not args.no_decode:
         dshape = wl.WORKLOADS[DECODE_WORKLOAD]
         dcfg = moe.config_from_shape(dshape)
         dws = torch.empty((moe.workspace_bytes(dcfg),), dtype=torch.uint8, device="cuda")
@@ -369,6 +452,7 @@ def run_ours(args, shape, world, rank, local):
         decode = {"workload": DECODE_WORKLOAD, "T": dshape.T, "ms_per_step": round(dms, 4),
                   "touched_experts": touched, "touched_weight_bytes": wbytes, "hbm_gbs": round(gbs, 1),
                   "peak_gbs": pk["hbm_gbs"], "frac": round(gbs / pk["hbm_gbs"], 4)}
+        del dws, dx, dy
 
     # end to end through the public calls with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -417,28 +501,41 @@ def run_ours(args, shape, world, rank, local):
 
     # CPU oracle baseline on a bounded sample (rank 0 at N = 1 only)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = {"x": x_host, "W_g": wl.gen_router(shape, 0), "logit_bias": lb_np, "weights": W_host}
-        n_tok = args.ref_tokens
-        t = oracle_sample_step(shape, host, n_tok)
-        cpu = {"value": n_tok / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": "first %d of %d tokens, one pass (fp32 router, fp64 experts), %.1f s" % (n_tok, shape.T, t)}
+    if want_cpu:
+        get_w = lambda name, e: wl.to_f64(W_host[(name, e)], shape.dtype)
+        cpu = cpu_record(shape, oracle_sample(shape, x_host[:n_tok], Wg_host, lb_np, get_w), n_tok)
 
     err = moe.get_device_error()
+    rec = {"value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(1e3 * total_s_max / args.steps, 4),
+           "dtype": shape.dtype, "config": workload_config(shape, world), "roofline": roof, "expert_gemm": eg,
+           "decode": decode, "stages_ms": stages, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
+           "clocks": clk.summary(), "device_error_word": err, "weights_drawn_s": round(gen_s, 1)}
+    del W, W_host, x, W_g, lb, ws, y, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args, shape, world, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pk = peaks()
+    head = measure_workload(args, shape, world, rank, pk, headline=True)
+    extras = {}
+    if world == 1 and not args.override:
+        for name in [w for w in args.workloads.split(",") if w and w != "none"]:
+            if name != shape.name:
+                extras[name] = measure_workload(args, wl.WORKLOADS[name], world, rank, pk, headline=False)
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s_max / args.steps, 4),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
-                "data": "synthetic (seeded: x ~ N(0,1), weights ~ N(0,1/fan_in); per-rank tokens, replicated weights)",
-                "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "d_ff": shape.d_ff, "E": shape.E,
-                           "k": shape.k, "scoring": shape.scoring, "n_shared": shape.n_shared,
-                           "tokens_per_gpu": shape.T, "parallelism": "replicas (token shards)" if world > 1 else "1 GPU",
-                           "l2": "flushed between steps (256 MiB write)"},
-                "roofline": roof,
-                "expert_gemm": {"tflops": round(expert_tflops, 2), "frac_of_peak": round(expert_tflops / peak, 4),
-                                "peak_tflops": peak},
-                "decode": decode, "stages_ms": stages, "e2e": e2e, "cpu_baseline": cpu,
-                "gpu_launches": launches, "clocks": clk.summary(), "device_error_word": err}
+        line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+                "data": "synthetic (seeded: x ~ N(0,1), weights ~ N(0,1/fan_in); per-rank tokens, replicated weights)"}
+        line.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step", "dtype")})
+        line["workloads"] = extras
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -453,7 +550,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--ref-tokens", type=int, default=64, help="tokens per CPU-oracle sample")
+    ap.add_argument("--workloads", default=",".join(EXTRA_WORKLOADS),
+                    help="further workloads measured after the headline one at N = 1 (comma list, or 'none')")
+    ap.add_argument("--ref-tokens", type=int, default=0, help="tokens per CPU-oracle sample (0: per workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -199,7 +199,8 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
      W1, W2  [E][d][d_ff] dtype     W3 [E][d_ff][d] dtype
      y_perm  [T*k][d] float32 out
    The intermediate h = (X W1) * SiLU(X W2) is kept in ws in dtype (bfloat16 for the
-   bfloat16 path). Experts with no rows are skipped and their weights are not read. */
+   bfloat16 path). Experts with no rows are skipped and their weights are not read.
+   Rows of y_perm from offsets[E] on are not written. */
 moe_status moe_experts(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                        const void* W1, const void* W2, const void* W3, float* y_perm,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -209,7 +210,8 @@ moe_status moe_experts(const moe_config* cfg, const void* x_perm, const int32_t*
    Page "8.6 - Mixture of Experts (MoE)", sections 2 (gate-weighted sum) and 4.1 (shared
    expert, gate 1); page "Mixture of Experts: What Actually Happens When a Token Hits the
    Router", Step 3 (scatter back).
-     y_perm [T*k][d] float32   inv_pos [T][k] int32   topk_gate [T][k] float32
+     y_perm [T*k][d] float32   inv_pos [T][k] int32 (-1: a dropped pair, adds nothing)
+     topk_gate [T][k] float32
      x [T][d] dtype, Ws1/Ws2/Ws3 as above: read only when cfg->n_shared > 0 (else may be NULL)
      y [T][d] dtype out */
 moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* inv_pos,
@@ -286,7 +288,14 @@ moe_status moe_forward_host_async(const moe_config* cfg, const void* x_host, con
 
 /* Waits for `stream`, then reads and clears the device error word of the current device.
    Returns MOE_OK, MOE_ERR_DEVICE (and the raw word in *word when word != NULL), or
-   MOE_ERR_CUDA when the wait itself failed. */
+   MOE_ERR_CUDA when the wait itself failed.  Bits of the word:
+     1 << 0  an expert id outside [0, E) in moe_dispatch's input (that pair was skipped)
+     1 << 1  grouped GEMM: offsets decreasing or beyond the rows of x_perm (clamped)
+     1 << 2, 1 << 3, 1 << 4  a pipeline wait of the TMA producer / MMA issuer / epilogue timed out
+     1 << 5  router: a non-finite logit
+     1 << 6  bounds-checking build only (libmoe_debug.so, compiled with MOE_DEBUG_BOUNDS): an
+             index read from offsets, perm_tok, inv_pos or pos_of was out of range (the access
+             was skipped; the normal build skips it silently) */
 moe_status moe_get_device_error(moe_stream_t stream, uint32_t* word);
 
 /* Testing aid for the failure detection of the pipelined GEMM kernels (the pages have no

@@ -16,14 +16,16 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restri
                                                           const int32_t* __restrict__ inv_pos,
                                                           const float* __restrict__ gate,
                                                           const float4* __restrict__ ys, int T, int d4, int k,
-                                                          long long rows_perm, void* __restrict__ y) {
+                                                          long long rows_perm, void* __restrict__ y, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   __shared__ int s_pos[32];
   __shared__ float s_g[32];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     if (threadIdx.x < k) {
-      s_pos[threadIdx.x] = __ldg(inv_pos + (size_t)t * k + threadIdx.x);
+      const int p = __ldg(inv_pos + (size_t)t * k + threadIdx.x);
+      debug_bounds(p >= -1 && p < rows_perm, err);   // -1: a pair dropped at dispatch
+      s_pos[threadIdx.x] = p;
       s_g[threadIdx.x] = __ldg(gate + (size_t)t * k + threadIdx.x);
     }
     __syncthreads();
@@ -31,7 +33,7 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restri
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < k; ++j) {
         const int p = s_pos[j];
-        if (p < 0 || p >= rows_perm) continue;   // only after an expert-id error (flagged)
+        if (p < 0 || p >= rows_perm) continue;   // a dropped pair, or a bad position (skipped)
         const float g = s_g[j];
         const float4 v = __ldg(y_perm + (size_t)p * d4 + c);
         acc.x = fmaf(g, v.x, acc.x);
@@ -59,7 +61,8 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
                                                              const int32_t* __restrict__ inv_pos,
                                                              const float* __restrict__ gate,
                                                              const float* __restrict__ ys, int T, int d, int k,
-                                                             long long rows_perm, void* __restrict__ y) {
+                                                             long long rows_perm, void* __restrict__ y,
+                                                             uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -67,6 +70,7 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
       float acc = 0.f;
       for (int j = 0; j < k; ++j) {
         const int p = __ldg(inv_pos + (size_t)t * k + j);
+        if (c == threadIdx.x) debug_bounds(p >= -1 && p < rows_perm, err);
         if (p < 0 || p >= rows_perm) continue;
         acc = fmaf(__ldg(gate + (size_t)t * k + j), __ldg(y_perm + (size_t)p * d + c), acc);
       }
@@ -82,7 +86,7 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
 }  // namespace
 
 cudaError_t combine(int dtype, const float* y_perm, const int32_t* inv_pos, const float* gate, const float* ys, int T,
-                    int d, int k, void* y, cudaStream_t st) {
+                    int d, int k, void* y, uint32_t* err, cudaStream_t st) {
   const long long rows_perm = (long long)T * k;
   const unsigned blocks = (unsigned)(T < 148 * 32 ? T : 148 * 32);
   const bool vec = (d % 4 == 0) && ((uintptr_t)y_perm % 16 == 0) && (!ys || (uintptr_t)ys % 16 == 0) &&
@@ -90,16 +94,16 @@ cudaError_t combine(int dtype, const float* y_perm, const int32_t* inv_pos, cons
   if (vec) {
     if (dtype == 1)
       MOE_RETURN_ON_ERROR(launch_k(combine_vec_kernel<true>, blocks, 256, 0, st, (const float4*)y_perm, inv_pos, gate,
-                         (const float4*)ys, T, d / 4, k, rows_perm, y));
+                         (const float4*)ys, T, d / 4, k, rows_perm, y, err));
     else
       MOE_RETURN_ON_ERROR(launch_k(combine_vec_kernel<false>, blocks, 256, 0, st, (const float4*)y_perm, inv_pos, gate,
-                         (const float4*)ys, T, d / 4, k, rows_perm, y));
+                         (const float4*)ys, T, d / 4, k, rows_perm, y, err));
   } else {
     if (dtype == 1)
-      MOE_RETURN_ON_ERROR(launch_k(combine_scalar_kernel<true>, blocks, 256, 0, st, y_perm, inv_pos, gate, ys, T, d, k, rows_perm, y));
+      MOE_RETURN_ON_ERROR(launch_k(combine_scalar_kernel<true>, blocks, 256, 0, st, y_perm, inv_pos, gate, ys, T, d, k, rows_perm, y, err));
     else
       MOE_RETURN_ON_ERROR(launch_k(combine_scalar_kernel<false>, blocks, 256, 0, st, y_perm, inv_pos, gate, ys, T, d, k, rows_perm,
-                         y));
+                         y, err));
   }
   ++g_launches;
   return cudaGetLastError();

@@ -18,6 +18,8 @@ enum : uint32_t {
   ERR_WAIT_MMA = 1u << 3,       // an MMA-issuer wait timed out
   ERR_WAIT_EPILOGUE = 1u << 4,  // an epilogue wait timed out
   ERR_ROUTE = 1u << 5,          // router: a non-finite logit was met
+  ERR_BOUNDS = 1u << 6,         // bounds-checking build only: an index read from offsets, perm_tok,
+                                // inv_pos or pos_of was out of range (the access was skipped)
 };
 
 // A pipeline wait gives up after this long (nanoseconds of %globaltimer).  Every wait in
@@ -26,6 +28,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
+}
+
+// Bounds-checking build (compiled with MOE_DEBUG_BOUNDS): flag ERR_BOUNDS when `ok` is false.
+// The normal build skips an out-of-range access at the same places without reporting it (or,
+// for indices that only the library itself computes, does not test them at all).
+__device__ __forceinline__ void debug_bounds(bool ok, uint32_t* err) {
+#ifdef MOE_DEBUG_BOUNDS
+  if (!ok) flag_error(err, ERR_BOUNDS);
+#else
+  (void)ok;
+  (void)err;
+#endif
 }
 
 __device__ __forceinline__ float bf16_to_float(uint16_t b) {

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
                                                              int n_chunks, int cap, const int32_t* __restrict__ chunk_base,
                                                              const int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ perm_tok,
-                                                             int32_t* __restrict__ inv_pos) {
+                                                             int32_t* __restrict__ inv_pos, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int sh[];
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
     if (i < N) {
       if (e >= 0) {
         const int pos = run[e] + __popc(m & lt);
+        debug_bounds(pos >= 0 && pos < N, err);
         if (pos - __ldg(offsets + e) < cap) {   // rank within the expert, in token order
           perm_tok[pos] = (int32_t)(i / k);
           inv_pos[i] = pos;
@@ -178,7 +179,8 @@ __global__ void __launch_bounds__(WARPS * 32) permute_kernel(const int32_t* __re
 template <typename V>
 __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, const int32_t* __restrict__ perm_tok,
                                                      long long rows, const int32_t* __restrict__ rows_dev,
-                                                     int vec_per_row, long long T, V* __restrict__ xp) {
+                                                     int vec_per_row, long long T, V* __restrict__ xp,
+                                                     uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
@@ -190,7 +192,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
   for (long long p = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; p < rows; p += warps) {
     const int t = __ldg(perm_tok + p);
     V* dst = xp + (size_t)p * vec_per_row;
-    if (t < 0 || t >= T) continue;   // only after an expert-id error; that is flagged already
+    const bool in_range = t >= 0 && t < T;
+    if (lane == 0) debug_bounds(in_range, err);
+    if (!in_range) continue;   // only after an expert-id error (flagged), or a caller's bad perm_tok
     const V* src = x + (size_t)t * vec_per_row;
     for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
@@ -198,9 +202,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
 
 // Small batches (T k <= SMALL_PAIRS, E <= SMALL_E), as decode steps produce: the histogram,
 // scan and permutation in one block of 1024 threads, with the same results as the three
-// kernels above.  Rounds of 1024 pairs in flattened order; warp w of a round takes its 32
-// pairs; a pair's rank within its expert is (pairs of the expert in earlier rounds) + (in
-// earlier warps of the round) + (lanes of its warp before it with the same expert).
+// kernels above, and no atomics either.  Rounds of 1024 pairs in flattened order; warp w of
+// a round takes its 32 pairs; a pair's rank within its expert is (pairs of the expert in
+// earlier rounds) + (in earlier warps of the round) + (lanes of its warp before it with the
+// same expert).
 constexpr int SMALL_PAIRS = 16384;
 constexpr int SMALL_E = 256;
 
@@ -216,15 +221,30 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
   __shared__ int off[SMALL_E + 1];
   __shared__ int wsum[33];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int e = tid; e < E; e += 1024) run[e] = 0;
-  __syncthreads();
+  // Histogram as in hist_kernel: each warp counts its pairs of every round in a private row of
+  // wc (the lowest lane of each group of equal experts adds the group's size), then thread e
+  // adds up expert e's column.
+  for (int x = lane; x < E; x += 32) wc[warp][x] = 0;
+  __syncwarp();
   bool bad = false;
-  for (int i = tid; i < N; i += 1024) {
-    const int e = __ldg(idx + i);
-    if (e < 0 || e >= E) bad = true;
-    else atomicAdd(&run[e], 1);   // counts only: the order of these additions does not matter
+  for (int base = 0; base < N; base += 1024) {
+    const int i = base + tid;
+    int e = -1;
+    if (i < N) {
+      e = __ldg(idx + i);
+      if (e < 0 || e >= E) { bad = true; e = -1; }
+    }
+    const unsigned m = __match_any_sync(FULL, e);
+    if (e >= 0 && lane == __ffs(m) - 1) wc[warp][e] += __popc(m);
+    __syncwarp();
   }
   if (bad) flag_error(err, ERR_EXPERT_ID);
+  __syncthreads();
+  for (int x = tid; x < E; x += 1024) {
+    int c = 0;
+    for (int w = 0; w < 32; ++w) c += wc[w][x];
+    run[x] = c;
+  }
   __syncthreads();
   // exclusive scan of the kept counts over the experts (E <= 256 < 1024 threads)
   const int kept = tid < E ? min(run[tid], cap) : 0;
@@ -290,6 +310,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
         const int rank = wc[warp][e] + __popc(m & lt);
         if (rank < cap) {
           pos = off[e] + rank;
+          debug_bounds(pos < N, err);
           perm_tok[pos] = (int32_t)(i / k);
         }
       }
@@ -323,27 +344,27 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int c
   MOE_RETURN_ON_ERROR(launch_k(scan_kernel, 1, 1024, 0, st, chunk_counts, n_chunks, E, S, cap, chunk_base, counts,
                                offsets));
   MOE_RETURN_ON_ERROR(launch_k(permute_kernel, blocks, WARPS * 32, shm, st, topk_idx, N, k, E, n_chunks, cap,
-                               chunk_base, offsets, perm_tok, inv_pos));
+                               chunk_base, offsets, perm_tok, inv_pos, err));
   g_launches += 3;
   if (launches) *launches += 3;
   return cudaGetLastError();
 }
 
 cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, const int32_t* rows_dev,
-                        int d, int elem_bytes, void* x_perm, cudaStream_t st) {
+                        int d, int elem_bytes, void* x_perm, uint32_t* err, cudaStream_t st) {
   const long long row_bytes = (long long)d * elem_bytes;
   const int threads = 256;
   long long want = (rows * 32 + threads - 1) / threads;
   const unsigned blocks = (unsigned)(want < 148LL * 16 ? want : 148LL * 16);
   if (row_bytes % 16 == 0 && ((uintptr_t)x % 16 == 0) && ((uintptr_t)x_perm % 16 == 0)) {
     MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint4>, blocks, threads, 0, st, (const uint4*)x, perm_tok, rows, rows_dev,
-                                 (int)(row_bytes / 16), T, (uint4*)x_perm));
+                                 (int)(row_bytes / 16), T, (uint4*)x_perm, err));
   } else if (row_bytes % 4 == 0) {
     MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint32_t>, blocks, threads, 0, st, (const uint32_t*)x, perm_tok, rows,
-                                 rows_dev, (int)(row_bytes / 4), T, (uint32_t*)x_perm));
+                                 rows_dev, (int)(row_bytes / 4), T, (uint32_t*)x_perm, err));
   } else {
     MOE_RETURN_ON_ERROR(launch_k(gather_kernel<uint16_t>, blocks, threads, 0, st, (const uint16_t*)x, perm_tok, rows,
-                                 rows_dev, (int)(row_bytes / 2), T, (uint16_t*)x_perm));
+                                 rows_dev, (int)(row_bytes / 2), T, (uint16_t*)x_perm, err));
   }
   ++g_launches;
   return cudaGetLastError();

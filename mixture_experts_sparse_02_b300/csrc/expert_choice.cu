@@ -169,7 +169,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) ec_combine_kernel(const float4* __restrict__ y_perm,
                                                          const int32_t* __restrict__ pos_of,
                                                          const float* __restrict__ gate, const float4* __restrict__ ys,
-                                                         int T, int E, int d4, void* __restrict__ y) {
+                                                         int T, int E, int d4, long long rows_perm, void* __restrict__ y,
+                                                         uint32_t* err) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int sh[];   // [E] positions, then [E] gates, of the experts that took t
@@ -182,7 +183,9 @@ __global__ void __launch_bounds__(256) ec_combine_kernel(const float4* __restric
     int cnt_before = 0;
     for (int base = 0; base < E; base += 256) {
       const int e = base + threadIdx.x;
-      const int p = e < E ? __ldg(pos_of + (size_t)t * E + e) : -1;
+      int p = e < E ? __ldg(pos_of + (size_t)t * E + e) : -1;
+      debug_bounds(p >= -1 && p < rows_perm, err);   // -1: expert e did not take t
+      if (p >= rows_perm) p = -1;                      // a bad position is skipped
       const unsigned bal = __ballot_sync(FULL, p >= 0);
       if (lane == 0) s_cnt[warp] = __popc(bal);
       __syncthreads();
@@ -258,15 +261,15 @@ cudaError_t ec_route(float* scores, const float* logit_bias, int T, int E, int m
 }
 
 cudaError_t ec_combine(int dtype, const float* y_perm, const int32_t* pos_of, const float* gate, const float* ys,
-                       int T, int E, int d, void* y, cudaStream_t st) {
+                       int T, int E, int d, long long rows_perm, void* y, uint32_t* err, cudaStream_t st) {
   const unsigned blocks = (unsigned)(T < 148 * 16 ? T : 148 * 16);
   const size_t smem = (size_t)E * 8;
   if (dtype == 1)
     MOE_RETURN_ON_ERROR(launch_k(ec_combine_kernel<true>, blocks, 256, smem, st, (const float4*)y_perm, pos_of, gate,
-                                 (const float4*)ys, T, E, d / 4, y));
+                                 (const float4*)ys, T, E, d / 4, rows_perm, y, err));
   else
     MOE_RETURN_ON_ERROR(launch_k(ec_combine_kernel<false>, blocks, 256, smem, st, (const float4*)y_perm, pos_of, gate,
-                                 (const float4*)ys, T, E, d / 4, y));
+                                 (const float4*)ys, T, E, d / 4, rows_perm, y, err));
   ++g_launches;
   return cudaGetLastError();
 }

@@ -105,6 +105,12 @@ __device__ __forceinline__ Tile decode_tile(const C& c, int G, int t) {
   return r;
 }
 
+// Bounds-checking build: the rows a tile stores lie inside the output ([0, rows_cap]); the group
+// table clamps the offsets it reads, so this only fails if that clamp is broken.
+__device__ __forceinline__ void debug_tile_rows(const Tile& tl, const GemmArgs& a) {
+  debug_bounds(tl.row0 >= 0 && tl.row0 <= tl.row_end && tl.row_end <= a.rows_cap, a.err);
+}
+
 // Warp-wide: the group table of a persistent grouped GEMM.  row_off[g] = offsets[g] clamped
 // to the output's rows (a violation is flagged), tile_start[g] = first tile of group g, with
 // row_tiles(rows) row tiles times n_tiles column tiles per non-empty group.
@@ -341,6 +347,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const Tile tl = decode_tile(c, G, t);
+      if (lane == 0) debug_tile_rows(tl, a);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       // Warp-uniform decision: the TMEM loads below are .sync.aligned.
@@ -547,6 +554,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     int it = 0;
     for (int t = cid; t < total; t += nclusters, ++it) {
       const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
+      if (lane == 0) debug_tile_rows(tl, a);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       const bool got = __all_sync(0xffffffffu, mbar_wait(&c.tfull[buf], use & 1u, &c.abort, a.wait_limit_ns));
@@ -603,8 +611,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 //     wide tile in buffer b borrows columns 0..31 of buffer 1 - b.  The epilogue drains a tile's
 //     tail and its columns 0..31 first and then arrives on thead[b], so the next tile's MMAs
 //     wait only for those two chunks (not the whole drain) before they overwrite them.
-// The SwiGLU epilogue passes X W2 from the warps that hold it (lanes 64-127) to the warps that
-// hold X W1 of the same features through a small shared-memory buffer, 32 tokens at a time.
+// The SwiGLU epilogue passes X W1 from the warps that hold it (lanes 0-63) to the warps that
+// hold X W2 of the same features through a small shared-memory buffer, 32 tokens at a time.
 // Synchronisation is otherwise that of the pair kernel above.
 namespace tpair {
 constexpr int TOK = 256;                           // tokens of a full tile (MMA N)
@@ -670,17 +678,17 @@ __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;"
 // Stores of one 32-column chunk: column j of the chunk is token base + j for j0 <= j < end (the
 // caller splits the chunk into runs on which the token map is affine).  One add, compare and
 // store per column, as few instructions as possible: these warps share issue slots with the
-// TMA producer and the MMA issuer.  SWIGLU: `xv` holds X W2 of the same features.
+// TMA producer and the MMA issuer.  SWIGLU: `r` holds X W2 and `xu` X W1 of the same features.
 template <int EPI>
 __device__ __forceinline__ void tpair_store_run(const GemmArgs& a, const Tile& tl, const uint32_t (&r)[32],
-                                                const float* xv, int lane, int f, int base, int j0, int end) {
+                                                const float* xu, int lane, int f, int base, int j0, int end) {
   if (EPI == EPI_SWIGLU) {
     uint16_t* p = reinterpret_cast<uint16_t*>(a.out) + (size_t)(tl.row0 + base) * a.ldo + f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       if (j >= j0 && j < end) {
-        const float u = __uint_as_float(r[j]);
-        const float v = xv[j * 32 + lane];
+        const float u = xu[j * 32 + lane];
+        const float v = __uint_as_float(r[j]);
         const float h = u * __fdividef(v, 1.0f + __expf(-v));
         p[(size_t)j * a.ldo] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
       }
@@ -708,28 +716,32 @@ __device__ __forceinline__ void tpair_store_chunk(const GemmArgs& a, const tpair
                                                   const uint32_t (&r)[32], int col0, bool tail, int q, int lane,
                                                   uint32_t rank, float* xchg) {
   int f;
-  float* xv = nullptr;
+  float* xu = nullptr;
   if (EPI == EPI_SWIGLU) {
+    // Warps 4-5 (TMEM lanes 0-63, X W1) hand their values to warps 6-7 (lanes 64-127, X W2 of
+    // the same features), which finish and store h: the TMA producer and the MMA issuer run on
+    // the same SM sub-partitions as warps 4 and 5 (warp w issues on sub-partition w % 4), so
+    // the SiLU and the stores go to the sub-partitions of the idle warps 2 and 3.
     f = tl.n_tile * 128 + 64 * (int)rank + 32 * (q & 1) + lane;
-    xv = xchg + (q & 1) * 32 * 32;
-    if (q >= 2) {
+    xu = xchg + (q & 1) * 32 * 32;
+    if (q < 2) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) xv[j * 32 + lane] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j) xu[j * 32 + lane] = __uint_as_float(r[j]);
     }
     epilogue_bar();
   } else {
     f = tl.n_tile * 256 + 128 * (int)rank + 32 * q + lane;
   }
-  if ((EPI != EPI_SWIGLU || q < 2) && f < a.N) {
+  if ((EPI != EPI_SWIGLU || q >= 2) && f < a.N) {
     if (!tail) {
       const int base = sh.main_token(col0);
       const int end = min(min(32, (sh.t16 ? tpair::TOK : sh.n16) - col0), sh.n - base);
-      tpair_store_run<EPI>(a, tl, r, xv, lane, f, base, 0, end);
+      tpair_store_run<EPI>(a, tl, r, xu, lane, f, base, 0, end);
     } else {
       const int split = sh.t16 / 2;
-      tpair_store_run<EPI>(a, tl, r, xv, lane, f, 128, 0, min(split, sh.n - 128));
+      tpair_store_run<EPI>(a, tl, r, xu, lane, f, 128, 0, min(split, sh.n - 128));
       const int base_b = sh.half + 128 - split;
-      tpair_store_run<EPI>(a, tl, r, xv, lane, f, base_b, split, min(sh.t16, sh.n - base_b));
+      tpair_store_run<EPI>(a, tl, r, xu, lane, f, base_b, split, min(sh.t16, sh.n - base_b));
     }
   }
   if (EPI == EPI_SWIGLU) epilogue_bar();
@@ -905,6 +917,7 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
     int it = 0;
     for (int t = cid; t < total; t += nclusters, ++it) {
       const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
+      if (lane == 0) debug_tile_rows(tl, a);
       const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);

@@ -80,7 +80,7 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int c
                              int32_t* inv_pos, uint32_t* err, cudaStream_t st, int* launches);
 // rows_dev (optional, device): the number of rows to copy, bounded by `rows`.
 cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, const int32_t* rows_dev,
-                        int d, int elem_bytes, void* x_perm, cudaStream_t st);
+                        int d, int elem_bytes, void* x_perm, uint32_t* err, cudaStream_t st);
 
 // ---- expert choice: scores [T][E] hold the router logits on entry and the per-token softmax
 // on return; every expert takes its m best tokens (perm_tok / gate by position, pos_of [T][E])
@@ -88,10 +88,10 @@ size_t ec_select_smem(int T);
 cudaError_t ec_route(float* scores, const float* logit_bias, int T, int E, int m, int32_t* offsets,
                      int32_t* perm_tok, float* gate, int32_t* pos_of, cudaStream_t st);
 cudaError_t ec_combine(int dtype, const float* y_perm, const int32_t* pos_of, const float* gate, const float* ys,
-                       int T, int E, int d, void* y, cudaStream_t st);
+                       int T, int E, int d, long long rows_perm, void* y, uint32_t* err, cudaStream_t st);
 
 // ---- combine
 cudaError_t combine(int dtype, const float* y_perm, const int32_t* inv_pos, const float* gate, const float* ys,
-                    int T, int d, int k, void* y, cudaStream_t st);
+                    int T, int d, int k, void* y, uint32_t* err, cudaStream_t st);
 
 }  // namespace moe

@@ -22,10 +22,15 @@ thread_local int g_launches = 0;
 // Device error word (one per device that loads the library).
 static __device__ uint32_t g_error_word;
 
+// Device address of g_error_word, looked up once per device with that device current (in host
+// code the symbol's name is only a host-side stand-in).  The table is shared by every host
+// thread, so the lookup and the cache are under a lock.
 static uint32_t* error_word() {
+  static std::mutex mu;
   static uint32_t* ptr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) ptr[dev] = static_cast<uint32_t*>(p);
@@ -200,7 +205,7 @@ static moe_status stage_dispatch(const moe_config& c, const int32_t* idx, const 
                                  int32_t* chunk_base, cudaStream_t st) {
   MOE_CUDA(dispatch_indices(idx, c.T, c.k, c.E, capacity_slots(c), chunk_counts, chunk_base, counts, offsets, perm,
                             inv, error_word(), st, nullptr));
-  return cuda_status(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, st));
+  return cuda_status(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, error_word(), st));
 }
 
 static moe_status stage_w12(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* W1,
@@ -240,12 +245,12 @@ static moe_status stage_shared(const moe_config& c, const void* x, const void* W
 
 static moe_status stage_combine(const moe_config& c, const float* y_perm, const int32_t* inv, const float* gate,
                                 const float* ys, void* y, cudaStream_t st) {
-  return cuda_status(combine(c.dtype, y_perm, inv, gate, ys, c.T, c.d, c.k, y, st));
+  return cuda_status(combine(c.dtype, y_perm, inv, gate, ys, c.T, c.d, c.k, y, error_word(), st));
 }
 
 static moe_status stage_combine_ec(const moe_config& c, const float* y_perm, const int32_t* pos_of, const float* gate,
                                    const float* ys, void* y, cudaStream_t st) {
-  return cuda_status(ec_combine(c.dtype, y_perm, pos_of, gate, ys, c.T, c.E, c.d, y, st));
+  return cuda_status(ec_combine(c.dtype, y_perm, pos_of, gate, ys, c.T, c.E, c.d, pairs_of(c), y, error_word(), st));
 }
 
 static moe_status check_weights(const moe_config& c, const void* W1, const void* W2, const void* W3) {
@@ -305,7 +310,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   if (ec) {
     MOE_TRY(stage_route_ec(c, x, W_g, lb, logits, offsets, perm, gate, inv, st));
     MOE_TRY(mark(1));
-    MOE_CUDA(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, st));
+    MOE_CUDA(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, error_word(), st));
   } else {
     MOE_TRY(stage_route(c, x, W_g, lb, sb, idx, gate, logits, st));
     MOE_TRY(mark(1));

@@ -3,7 +3,8 @@
 Every call takes torch tensors on the current CUDA device (or plain integer addresses) and
 forwards their data pointers to the C ABI; all computation happens in the library's CUDA
 kernels.  Importing this module fails if libmoe.so has not been built: there is no CPU or
-PyTorch fallback.
+PyTorch fallback.  With the environment variable MOE_LIBRARY=debug it loads the
+bounds-checking build libmoe_debug.so instead (same calls; see build.py).
 """
 from __future__ import annotations
 
@@ -12,11 +13,12 @@ import os
 from typing import Optional, Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe.so")
+_DEBUG = os.environ.get("MOE_LIBRARY", "") == "debug"
+LIB_PATH = os.path.join(_HERE, "libmoe_debug.so" if _DEBUG else "libmoe.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libmoe.so is missing (%s); build it with "
-                      "`python -m mixture_experts_sparse_02_b300.build`" % LIB_PATH)
+    raise ImportError("%s is missing; build it with `python -m mixture_experts_sparse_02_b300.build%s`"
+                      % (LIB_PATH, " --debug-bounds" if _DEBUG else ""))
 _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)

@@ -1,8 +1,9 @@
 """Helpers shared by the GPU tests: upload seeded inputs, run the library, compare to the oracle."""
 from __future__ import annotations
 
+import os
 from concurrent.futures import ThreadPoolExecutor
-from typing import Dict, Iterable, Optional
+from typing import Dict, Iterable, List, Optional, Tuple
 
 import numpy as np
 import pytest
@@ -96,15 +97,15 @@ def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
 
 
 def layer_out_err(got: np.ndarray, ref: np.ndarray, shape) -> float:
-    """Error of the layer output y against the oracle, in units of rms(ref).
+    """Error of a stored output (the layer output y, or the expert outputs y_perm) against the
+    oracle, in units of rms(ref).
 
-    float32 layers: max|y - ref| / rms(ref).  bfloat16 layers: y is stored in bfloat16, so
-    it carries up to half a bfloat16 ulp of its own value beyond any arithmetic error; that
-    rounding alone reaches ~2.4% of rms(ref) at the largest outputs of these shapes.  The
-    rule is therefore applied to the value before that final rounding, through the lower
-    bound max(|y - ref| - ulp(y)/2) / rms(ref): it can only fail if the unrounded value
-    misses the rule.  Expert outputs before rounding (y_perm, float32) are checked with the
-    plain rule."""
+    float32 layers: max|y - ref| / rms(ref).  bfloat16 layers: the value is stored in
+    bfloat16, so it carries up to half a bfloat16 ulp of its own value beyond any arithmetic
+    error; that rounding alone reaches ~2.4% of rms(ref) at the largest outputs of these
+    shapes.  The rule is therefore applied to the value before that final rounding, through
+    the lower bound max(|y - ref| - ulp(y)/2) / rms(ref): it can only fail if the unrounded
+    value misses the rule."""
     got = np.asarray(got, np.float64)
     rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
     d = np.abs(got - ref)
@@ -115,3 +116,27 @@ def layer_out_err(got: np.ndarray, ref: np.ndarray, shape) -> float:
 
 def y_tol(shape) -> float:
     return BF16_TOL if shape.dtype == "bf16" else F32_TOL
+
+
+# (test, what, raw max|err|/rms, figure the rule is applied to, tolerance) of every check_close
+# call in this session; tests/conftest.py prints a summary at the end of the run.
+RECORDS: List[Tuple[str, str, float, float, float]] = []
+
+
+def check_close(got, ref: np.ndarray, shape, what: str = "y") -> Tuple[float, float]:
+    """Assert the output rule of the layer's dtype on a result (device tensor or array) against
+    the oracle and record both figures: the raw max|err|/rms(ref), and the figure the rule is
+    applied to (a bfloat16 tensor: after half a bfloat16 ulp of the stored value, see
+    layer_out_err; a float32 tensor, such as y_perm: the raw figure)."""
+    stored_bf16 = isinstance(got, torch.Tensor) and got.dtype == torch.bfloat16
+    if isinstance(got, torch.Tensor):
+        got = dev_to_f64(got)
+    got = np.asarray(got, np.float64)
+    raw = max_rel_err(got, ref)
+    err = layer_out_err(got, ref, shape) if stored_bf16 else raw
+    tol = y_tol(shape)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    RECORDS.append((test, what, raw, err, tol))
+    assert err <= tol, ("%s: max|err| = %.3g rms(ref) raw, %.3g rms(ref) after half a bf16 ulp of the stored "
+                        "value; tolerance %g" % (what, raw, err, tol))
+    return raw, err

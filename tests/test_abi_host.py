@@ -27,9 +27,11 @@ def declared_functions():
 def test_exports_every_declared_symbol(moe):
     names = declared_functions()
     assert len(names) >= 11
-    lib = ctypes.CDLL(moe.LIB_PATH)
-    for n in names:
-        assert hasattr(lib, n), n
+    from mixture_experts_sparse_02_b300 import build
+    for path in (moe.LIB_PATH, build.build(debug_bounds=True)):   # the normal and the bounds-checking build
+        lib = ctypes.CDLL(path)
+        for n in names:
+            assert hasattr(lib, n), (path, n)
     assert set(names) == set(moe.EXPORTS)
 
 
@@ -45,7 +47,7 @@ def test_workspace_bytes(moe):
     assert moe.workspace_bytes(moe.config(64, 4096, 14336, 8, 2)) < big
     assert moe.workspace_bytes(moe.config(4, 64, 64, 8, 9)) == 0        # k > E: invalid
     s = moe.workspace_bytes(moe.config(8192, 7168, 2048, 256, 8, scoring="sigmoid", n_shared=1, d_ff_shared=2048))
-    assert s > 8192 * 8 * 7168 * (2 + 4)
+    assert s > 8192 * 8 * 7168 * (2 + 4)            # x_perm (bf16) and y_perm (float32)
 
 
 FAKE = 0x100000  # a 16-byte aligned address that is never dereferenced: the checks return first
@@ -119,3 +121,22 @@ def test_update_sel_bias_argument_errors(moe):
     with pytest.raises(moe.MoEError) as e:
         moe.update_sel_bias(moe.config(16, 64, 64, 8, 9), FAKE, 0.1, FAKE, stream=0)
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_static_dispatch_rejects_sizes_beyond_its_array(moe):
+    # ceil(T k / 256) * E = 513 * 256 = 131328 > 131072: refused before anything is launched
+    cfg = moe.config(16384 + 32, 64, 64, 256, 8)
+    with pytest.raises(moe.MoEError) as e:
+        moe.dispatch_static(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, stream=0)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_expert_choice_rejects_token_choice_calls(moe):
+    cfg = moe.config(64, 64, 64, 8, 2, scoring="expert_choice")
+    with pytest.raises(moe.MoEError) as e:
+        moe.dispatch(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoEError) as e:
+        moe.dispatch_static(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, stream=0)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    assert _fwd(moe, cfg, topk_idx_out=FAKE) == moe.MOE_ERR_UNSUPPORTED

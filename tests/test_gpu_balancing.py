@@ -12,8 +12,7 @@ import workloads as wl
 from oracle import Case
 from oracle import moe_oracle as orc
 
-from gpu_util import (GATE_ATOL, dev_to_f64, layer_out_err, require_cuda, tdtype, to_dev, upload_experts,
-                      y_tol)
+from gpu_util import GATE_ATOL, check_close, require_cuda, tdtype, to_dev, upload_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +60,7 @@ def test_route_and_forward_with_selection_bias(moe, shape, std):
     assert moe.get_device_error() == 0
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
     assert np.array_equal(counts.cpu().numpy(), ref["counts"])
-    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    check_close(y, ref["y"], s)
 
 
 @pytest.mark.parametrize("T,k,E", [(10, 2, 4), (4096, 2, 8), (8192, 8, 256), (333, 6, 64), (7, 1, 3)])
@@ -138,7 +137,7 @@ def test_switch_style_gates(moe, shape):
     moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y, ws, logit_bias=lb, topk_idx_out=idx)
     assert moe.get_device_error() == 0
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
-    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    check_close(y, ref["y"], s)
 
 
 STATS_SHAPES = [

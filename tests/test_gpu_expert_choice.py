@@ -12,8 +12,7 @@ import workloads as wl
 from oracle import Case
 from oracle import moe_oracle as orc
 
-from gpu_util import (GATE_ATOL, dev_to_f64, layer_out_err, max_rel_err, require_cuda, tdtype, to_dev,
-                      upload_experts, y_tol)
+from gpu_util import GATE_ATOL, check_close, require_cuda, tdtype, to_dev, upload_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -63,32 +62,21 @@ def test_expert_choice(moe, shape):
     xp = to_dev(case.x[ref["perm_tok"]], s)
     y_perm = torch.empty((s.E * m, s.d), dtype=torch.float32, device="cuda")
     moe.experts(cfg, xp, offsets, W["W1"], W["W2"], W["W3"], y_perm, ws)
-    assert max_rel_err(dev_to_f64(y_perm), ref["y_perm"]) <= y_tol(s)
+    check_close(y_perm, ref["y_perm"], s, "y_perm")
     y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
     moe.combine_expert_choice(cfg, torch.from_numpy(ref["y_perm"].astype(np.float32)).cuda(),
                               torch.from_numpy(ref["gate"].astype(np.float32)).cuda(),
                               torch.from_numpy(ref["pos_of"]).cuda(), y, x=x, Ws1=W.get("Ws1"), Ws2=W.get("Ws2"),
                               Ws3=W.get("Ws3"), ws=ws)
-    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    check_close(y, ref["y"], s)
     # the whole layer through moe_forward, twice: identical
     for _ in range(2):
         y2 = torch.empty_like(y)
         moe.forward(cfg, x, Wg, W["W1"], W["W2"], W["W3"], y2, ws, logit_bias=lb, Ws1=W.get("Ws1"),
                     Ws2=W.get("Ws2"), Ws3=W.get("Ws3"))
         assert moe.get_device_error() == 0
-        assert layer_out_err(dev_to_f64(y2), ref["y"], s) <= y_tol(s)
+        check_close(y2, ref["y"], s)
     assert moe.last_launch_count() == 3 + 1 + 2 + 2 * s.n_shared + 1
-
-
-def test_expert_choice_rejects_token_choice_calls(moe):
-    cfg = moe.config(64, 64, 64, 8, 2, scoring="expert_choice")
-    fake = 0x100000
-    with pytest.raises(moe.MoEError) as e:
-        moe.dispatch(cfg, fake, fake, fake, fake, fake, fake, fake, fake, ws_bytes=1 << 30, stream=0)
-    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
-    with pytest.raises(moe.MoEError) as e:
-        moe.forward(cfg, fake, fake, fake, fake, fake, fake, fake, ws_bytes=1 << 40, topk_idx_out=fake, stream=0)
-    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_expert_choice_full_size_mixtral_shaped(moe):
@@ -124,4 +112,4 @@ def test_expert_choice_full_size_mixtral_shaped(moe):
         if rows.size:
             fe = orc.swiglu_expert(xs[rows], get_w("W1", e), get_w("W2", e), get_w("W3", e))
             y_ref[rows] += r["scores"][sample[rows], e][:, None] * fe
-    assert layer_out_err(dev_to_f64(y[torch.from_numpy(sample).cuda()]), y_ref, s) <= y_tol(s)
+    check_close(y[torch.from_numpy(sample).cuda()], y_ref, s, "y (sampled tokens)")

@@ -14,8 +14,8 @@ import workloads as wl
 from oracle import Case
 from oracle import moe_oracle as orc
 
-from gpu_util import (GATE_ATOL, dev_to_f64, from_dev_stored, host_weight_fn, layer_out_err,
-                      max_rel_err, require_cuda, tdtype, to_dev, upload_experts, y_tol)
+from gpu_util import (GATE_ATOL, check_close, dev_to_f64, from_dev_stored, host_weight_fn, require_cuda, tdtype,
+                      to_dev, upload_experts)
 
 pytestmark = pytest.mark.gpu
 
@@ -102,8 +102,7 @@ def test_forward_small(moe, shape):
     y, idx, counts = _forward(moe, case, W, _device_inputs(case))
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
     assert np.array_equal(counts.cpu().numpy(), ref["counts"])
-    err = layer_out_err(dev_to_f64(y), ref["y"], shape)
-    assert err <= y_tol(shape), err
+    check_close(y, ref["y"], shape)
     # run-to-run identical
     y2, _, _ = _forward(moe, case, W, _device_inputs(case))
     assert torch.equal(y, y2)
@@ -143,7 +142,7 @@ def test_stages_small(moe, shape):
     off_ref = torch.from_numpy(ref["offsets"]).cuda()
     y_perm = torch.empty((s.T * s.k, s.d), dtype=torch.float32, device="cuda")
     moe.experts(cfg, xp_ref, off_ref, W["W1"], W["W2"], W["W3"], y_perm, ws)
-    assert max_rel_err(dev_to_f64(y_perm), ref["y_perm"]) <= y_tol(s)
+    check_close(y_perm, ref["y_perm"], s, "y_perm")
     # combine (oracle y_perm, inv_pos, gates in)
     yp_ref = torch.from_numpy(ref["y_perm"].astype(np.float32)).cuda()
     inv_ref = torch.from_numpy(ref["inv_pos"]).cuda()
@@ -151,7 +150,7 @@ def test_stages_small(moe, shape):
     y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
     moe.combine(cfg, yp_ref, inv_ref, g_ref, y, x=din["x"], Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"),
                 ws=ws)
-    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    check_close(y, ref["y"], s)
     assert moe.get_device_error() == 0
 
 
@@ -172,13 +171,13 @@ def test_gemm_kernels(moe, shape, variant, monkeypatch):
     y_perm = torch.empty((s.T * s.k, s.d), dtype=torch.float32, device="cuda")
     moe.experts(cfg, xp_ref, off_ref, W["W1"], W["W2"], W["W3"], y_perm, ws)
     assert moe.get_device_error() == 0
-    assert max_rel_err(dev_to_f64(y_perm), ref["y_perm"]) <= y_tol(s)
+    check_close(y_perm, ref["y_perm"], s, "y_perm")
     y_perm2 = torch.empty_like(y_perm)
     moe.experts(cfg, xp_ref, off_ref, W["W1"], W["W2"], W["W3"], y_perm2, ws)
     assert torch.equal(y_perm, y_perm2)
     y, idx, _ = _forward(moe, case, W, _device_inputs(case))
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
-    assert layer_out_err(dev_to_f64(y), ref["y"], s) <= y_tol(s)
+    check_close(y, ref["y"], s)
 
 
 @pytest.mark.parametrize("variant", ["single", "pair", "tpair", "tpairw"])
@@ -200,7 +199,7 @@ def test_gemm_tile_boundaries(moe, variant, monkeypatch):
     assert moe.get_device_error() == 0
     got = dev_to_f64(y_perm)
     assert np.isfinite(got).all()           # every row written
-    assert max_rel_err(got, ref) <= y_tol(s)
+    check_close(got, ref, s, "y_perm")
 
 
 FULL = ["mixtral_prefill", "mixtral_decode", "hunyuan_a13b", "deepseek_v3"]
@@ -218,14 +217,34 @@ def _sample_tokens(idx, counts, T, n_random, seed=1):
     return np.unique(np.array(pick, dtype=np.int64))
 
 
+def _check_blocks(counts, T):
+    """Expert blocks whose every row is compared at full size: the hottest and the coldest
+    non-empty expert, and, where the layer has them, one block of 257..288 rows (one wide
+    token tile) and one of at most 256 rows (one token tile).  Decode-sized layers: all."""
+    nz = np.nonzero(counts)[0]
+    if T <= 64:
+        return [int(e) for e in nz]
+    pick = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])]
+    for lo, hi in ((257, 288), (1, 256)):
+        cand = [int(e) for e in nz if lo <= counts[e] <= hi and int(e) not in pick]
+        if cand:
+            pick.append(cand[len(cand) // 2])
+    return pick
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size(moe, name):
+    """The five workloads at full size through the same moe_forward call that bench.py times:
+    routing, counts, offsets and the permutation bit-exact; the layer output on sampled tokens;
+    and every row of whole expert blocks of the experts call (the hottest, the coldest, a
+    wide-tile block, a one-tile block) against float64 evaluations of those blocks."""
     s = wl.WORKLOADS[name]
     case = Case(s, 0)
     r = case.route()
     dsp = orc.dispatch(r["idx"], s.E)
     sample = _sample_tokens(r["idx"], dsp["counts"], s.T, 12 if s.E >= 256 else 24)
-    W = upload_experts(s, 0, keep=np.unique(r["idx"][sample]))
+    blocks = _check_blocks(dsp["counts"], s.T)
+    W = upload_experts(s, 0, keep=set(np.unique(r["idx"][sample]).tolist()) | set(blocks))
     din = _device_inputs(case)
     y, idx, counts = _forward(moe, case, W, din)
     assert np.array_equal(idx.cpu().numpy(), r["idx"])
@@ -233,8 +252,7 @@ def test_full_size(moe, name):
     get_w = host_weight_fn(W["host"], s)
     x64 = case.f64(case.x[sample])
     y_ref = orc.forward_tokens(x64, r["idx"][sample], r["gate"][sample], get_w, s.n_shared)
-    err = layer_out_err(dev_to_f64(y[torch.from_numpy(sample).cuda()]), y_ref, s)
-    assert err <= y_tol(s), err
+    check_close(y[torch.from_numpy(sample).cuda()], y_ref, s, "y (%d sampled tokens)" % len(sample))
     # routing and dispatch outputs of the separate calls, at full size
     cfg = moe.config_from_shape(s)
     ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
@@ -251,6 +269,16 @@ def test_full_size(moe, name):
     assert np.array_equal(inv.cpu().numpy(), dsp["inv_pos"])
     rows = np.random.default_rng(2).choice(s.T * s.k, size=min(64, s.T * s.k), replace=False)
     assert np.array_equal(from_dev_stored(x_perm[torch.from_numpy(rows).cuda()], s), case.x[dsp["perm_tok"][rows]])
+    # the experts call at full size (every expert block, the kernels bench.py runs); every row of
+    # the chosen blocks against the oracle's float64 evaluation of the block
+    y_perm = torch.full((s.T * s.k, s.d), float("nan"), dtype=torch.float32, device="cuda")
+    moe.experts(cfg, x_perm, offsets, W["W1"], W["W2"], W["W3"], y_perm, ws)
+    assert moe.get_device_error() == 0
+    for e in blocks:
+        a, b = int(dsp["offsets"][e]), int(dsp["offsets"][e + 1])
+        ref_rows = orc.swiglu_expert(case.f64(case.x[dsp["perm_tok"][a:b]]), get_w("W1", e), get_w("W2", e),
+                                     get_w("W3", e))
+        check_close(y_perm[a:b], ref_rows, s, "y_perm of expert %d (%d rows)" % (e, b - a))
     assert moe.get_device_error() == 0
 
 
