@@ -35,6 +35,7 @@
 // limit) and on a timeout sets the device error word and unwinds.
 #include <cudaTypedefs.h>
 #include <atomic>
+#include <mutex>
 #include <stdlib.h>
 #include <string.h>
 
@@ -376,6 +377,78 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
+// ------------------------------------------------------------------------- dynamic tile schedule
+// The CTA-pair kernels take their tiles dynamically.  One thread of CTA 0 (the scheduler) takes
+// tile ids in increasing order from a counter in global memory shared by all clusters of the
+// launch and hands each to both CTAs of its pair through a ring of SCHED_RING slots; every role
+// of the pair takes the same sequence from the ring.  The scheduler takes the next id only when
+// the pair's TMA producer starts its current tile, so each pair holds one id ahead and the
+// tiles running at any moment are a narrow window of consecutive ids: the row (token) tiles of
+// one expert's column (feature) tile, which share a weight slice, start at about the same time
+// and find it in L2, and so do the column tiles that share rows.  A static round-robin schedule
+// lets clusters drift apart over many rounds (tiles differ in length: token tiles of 16..288
+// rows, DRAM and power stalls), and each then streams the slice from HBM; handing out ids
+// further ahead scatters the running tiles the same way.  A tile's result does not depend on
+// which cluster computes it.
+constexpr int SCHED_RING = 4;
+// Roles that take every tile id from the ring: in CTA 0 the TMA producer, the MMA issuer and
+// four epilogue warps; in CTA 1 the TMA producer and four epilogue warps.
+constexpr int SCHED_CONSUMERS = 11;
+
+struct Sched {
+  uint64_t full[SCHED_RING];    // slot holds the next tile id (arrived by the scheduler)
+  uint64_t empty[SCHED_RING];   // CTA 0 only: every consumer has read the slot
+  uint64_t taken;               // CTA 0 only: its TMA producer has taken the next tile id
+  int ring[SCHED_RING];
+};
+
+__device__ __forceinline__ void sched_init(Sched& s) {
+  for (int i = 0; i < SCHED_RING; ++i) {
+    mbar_init(&s.full[i], 1);
+    mbar_init(&s.empty[i], SCHED_CONSUMERS);
+  }
+  mbar_init(&s.taken, 1);
+}
+
+// Consumer side: wait for ring slot i % SCHED_RING and return its tile id (-1: no more tiles,
+// -2: the wait failed).  The caller releases the slot with sched_release once it has read it.
+__device__ __forceinline__ int sched_peek(Sched& s, volatile int* abort, int i, unsigned long long limit) {
+  const int slot = i % SCHED_RING;
+  if (!mbar_wait_acq_cluster(&s.full[slot], (uint32_t)(i / SCHED_RING) & 1u, abort, limit)) return -2;
+  return s.ring[slot];
+}
+
+__device__ __forceinline__ void sched_release(Sched& s, int i) {
+  mbar_arrive_cluster(mapa_shared(smem_addr(&s.empty[i % SCHED_RING]), 0));
+}
+
+// Scheduler (one thread of CTA 0): hands out tile ids until they run out, then counts its
+// cluster as finished; the last cluster to finish resets the counters for the next launch.
+// Id i + 1 is taken once CTA 0's producer has taken id i (`taken`) and its ring slot is free.
+__device__ __forceinline__ void sched_run(Sched& s, volatile int* abort, const GemmArgs& a, int total,
+                                          int nclusters) {
+  for (int i = 0;; ++i) {
+    const int slot = i % SCHED_RING;
+    if ((i >= 1 && !mbar_wait(&s.taken, (uint32_t)(i - 1) & 1u, abort, a.wait_limit_ns)) ||
+        (i >= SCHED_RING && !mbar_wait(&s.empty[slot], (uint32_t)(i / SCHED_RING - 1) & 1u, abort, a.wait_limit_ns))) {
+      flag_error(a.err, ERR_WAIT_PRODUCER);
+      *abort = 1;
+      break;
+    }
+    int t = atomicAdd(a.tile_ctr, 1);
+    if (t >= total) t = -1;
+    s.ring[slot] = t;
+    st_shared_cluster(mapa_shared(smem_addr(&s.ring[slot]), 1), t);
+    mbar_arrive(&s.full[slot]);
+    mbar_arrive_cluster(mapa_shared(smem_addr(&s.full[slot]), 1));   // releases the store above
+    if (t < 0) break;
+  }
+  if (atomicAdd(a.tile_ctr + 1, 1) == nclusters - 1) {
+    atomicExch(a.tile_ctr, 0);
+    atomicExch(a.tile_ctr + 1, 0);
+  }
+}
+
 // ------------------------------------------------------------------------- CTA-pair kernel
 // The same grouped GEMM with one tcgen05.mma.cta_group::2 per 256 x 256 x 16 step shared by the
 // two CTAs of a cluster.  CTA r of the pair loads rows row0 + 128 r .. + 127 of A and MMA
@@ -404,6 +477,7 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  Sched sched;
   uint32_t tmem_base;
   volatile int abort;
   int tile_start[MAX_GROUPS + 1];
@@ -436,8 +510,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const int lane = threadIdx.x & 31;
   const int G = a.offsets ? a.G : 1;
   const uint32_t rank = cluster_ctarank();
-  const int cid = (int)(blockIdx.x >> 1);        // clusters are pairs of consecutive blocks
-  const int nclusters = (int)(gridDim.x >> 1);
+  const int nclusters = (int)(gridDim.x >> 1);   // clusters are pairs of consecutive blocks
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -448,6 +521,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       mbar_init(&c.tfull[b], 1);
       mbar_init(&c.tempty[b], 8);
     }
+    sched_init(c.sched);
     mbar_init(&c.drain, 1);
     c.abort = 0;
     fence_barrier_init_cluster();
@@ -473,7 +547,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       // ---------------------------------------------------------------- TMA producer (both CTAs)
       int s = 0;
       uint32_t phase = 0;
-      for (int t = a.starve ? total : cid; t < total; t += nclusters) {
+      for (int i = 0;; ++i) {
+        const int t = sched_peek(c.sched, &c.abort, i, a.wait_limit_ns);
+        sched_release(c.sched, i);
+        if (rank == 0) mbar_arrive(&c.sched.taken);   // the scheduler may take the next id
+        if (t == -2) {
+          flag_error(a.err, ERR_WAIT_PRODUCER);
+          c.abort = 1;
+          break;
+        }
+        if (t < 0) break;
+        if (a.starve) continue;   // test hook: no copies, so the MMA and epilogue waits run out
         const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
         const int z = a.offsets ? tl.g : a.b_z;
         const int arow = tl.row0 + (int)rank * pair::BM;
@@ -515,7 +599,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       bool ok = true;
       const uint64_t ad_base = sdesc_sw128(smem_addr(stages), 16, 1024);   // stage 0, as above
       const uint64_t bd_base = sdesc_sw128(smem_addr(stages) + pair::A_TILE, B_SUB, 1024);
-      for (int t = cid; t < total && ok; t += nclusters, ++it) {
+      for (;; ++it) {
+        const int t = sched_peek(c.sched, &c.abort, it, a.wait_limit_ns);
+        sched_release(c.sched, it);
+        if (t == -2) { ok = false; break; }
+        if (t < 0) break;
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait(&c.tempty[buf], (use & 1u) ^ 1u, &c.abort, a.wait_limit_ns)) { ok = false; break; }
@@ -546,13 +634,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         mbar_wait(&c.drain, 0, &never, a.wait_limit_ns);
       }
     }
+  } else if (warp == 3) {
+    if (lane == 0 && rank == 0) sched_run(c.sched, &c.abort, a, total, nclusters);   // ---- tile scheduler (CTA 0)
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     const uint32_t tempty0 = mapa_shared(smem_addr(&c.tempty[0]), 0);
     const uint32_t tempty1 = mapa_shared(smem_addr(&c.tempty[1]), 0);
-    int it = 0;
-    for (int t = cid; t < total; t += nclusters, ++it) {
+    for (int it = 0;; ++it) {
+      const int t_lane = sched_peek(c.sched, &c.abort, it, a.wait_limit_ns);
+      const bool fed = __all_sync(0xffffffffu, t_lane != -2);
+      const int t = __shfl_sync(0xffffffffu, t_lane, 0);
+      __syncwarp();
+      if (lane == 0) sched_release(c.sched, it);
+      if (!fed) {
+        if (lane == 0) flag_error(a.err, ERR_WAIT_EPILOGUE);
+        c.abort = 1;
+        break;
+      }
+      if (t < 0) break;
       const Tile tl = decode_tile<pair::PAIR_M>(c, G, t);
       if (lane == 0) debug_tile_rows(tl, a);
       const int buf = it & 1;
@@ -622,7 +722,7 @@ constexpr int A_BYTES = 2 * B_SUB;                 // 16 KB
 constexpr int B_MAIN = BM * BK * 2;                // 16 KB: 128 token rows x 64 k
 constexpr int B_TAIL_ROWS = WIDE_ROWS / 2;         // 16 rows per CTA for the tail MMA
 constexpr int B_TAIL = B_TAIL_ROWS * BK * 2;       // 2 KB
-constexpr int XCHG_FLOATS = 2 * 32 * 32;           // X W2 of 64 features x 32 tokens
+constexpr int XCHG_FLOATS = 2 * 32 * 32;           // X W1 of 64 features x 32 tokens
 constexpr uint32_t IDESC_BASE = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(256 >> 4) << 24);
 
 // Instruction descriptor: D f32, A and B bf16, A MN-major, B K-major, M = 256, N = n.
@@ -635,6 +735,7 @@ struct Ctrl {
   uint64_t tempty[2];
   uint64_t thead[2];
   uint64_t drain;
+  Sched sched;
   uint32_t tmem_base;
   volatile int abort;
   int ep_ok[4];
@@ -765,7 +866,6 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
   const int lane = threadIdx.x & 31;
   const int G = a.offsets ? a.G : 1;
   const uint32_t rank = cluster_ctarank();
-  const int cid = (int)(blockIdx.x >> 1);
   const int nclusters = (int)(gridDim.x >> 1);
   const int feat_per_tile = EPI == EPI_SWIGLU ? 128 : 256;   // output features of one pair tile
 
@@ -779,6 +879,7 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       mbar_init(&c.tempty[b], 8);
       mbar_init(&c.thead[b], 8);
     }
+    sched_init(c.sched);
     mbar_init(&c.drain, 1);
     c.abort = 0;
     fence_barrier_init_cluster();
@@ -805,7 +906,17 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       // ---------------------------------------------------------------- TMA producer (both CTAs)
       int s = 0;
       uint32_t phase = 0;
-      for (int t = a.starve ? total : cid; t < total; t += nclusters) {
+      for (int i = 0;; ++i) {
+        const int t = sched_peek(c.sched, &c.abort, i, a.wait_limit_ns);
+        sched_release(c.sched, i);
+        if (rank == 0) mbar_arrive(&c.sched.taken);   // the scheduler may take the next id
+        if (t == -2) {
+          flag_error(a.err, ERR_WAIT_PRODUCER);
+          c.abort = 1;
+          break;
+        }
+        if (t < 0) break;
+        if (a.starve) continue;   // test hook: no copies, so the MMA and epilogue waits run out
         const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
         const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
         const int z = a.offsets ? tl.g : a.b_z;
@@ -849,7 +960,11 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
       bool prev_wide = false;
       const uint64_t ad_base = sdesc_sw128(smem_addr(stages), B_SUB, 1024);
       const uint64_t bd_base = sdesc_sw128(smem_addr(stages) + tpair::A_BYTES, 16, 1024);
-      for (int t = cid; t < total && ok; t += nclusters, ++it) {
+      for (;; ++it) {
+        const int t = sched_peek(c.sched, &c.abort, it, a.wait_limit_ns);
+        sched_release(c.sched, it);
+        if (t == -2) { ok = false; break; }
+        if (t < 0) break;
         const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
         const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
         const bool wide = WIDE && sh.t16 != 0;
@@ -907,6 +1022,8 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
         mbar_wait(&c.drain, 0, &never, a.wait_limit_ns);
       }
     }
+  } else if (warp == 3) {
+    if (lane == 0 && rank == 0) sched_run(c.sched, &c.abort, a, total, nclusters);   // ---- tile scheduler (CTA 0)
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;   // TMEM lanes 32 q .. 32 q + 31
@@ -914,8 +1031,25 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
     const uint32_t tempty1 = mapa_shared(smem_addr(&c.tempty[1]), 0);
     const uint32_t thead0 = mapa_shared(smem_addr(&c.thead[0]), 0);
     const uint32_t thead1 = mapa_shared(smem_addr(&c.thead[1]), 0);
-    int it = 0;
-    for (int t = cid; t < total; t += nclusters, ++it) {
+    for (int it = 0;; ++it) {
+      // The four warps take the same decision: they meet at unbounded named barriers below.
+      const int t_lane = sched_peek(c.sched, &c.abort, it, a.wait_limit_ns);
+      const bool mine_fed = __all_sync(0xffffffffu, t_lane != -2);
+      const int t = __shfl_sync(0xffffffffu, t_lane, 0);
+      __syncwarp();
+      if (lane == 0) {
+        sched_release(c.sched, it);
+        c.ep_ok[q] = mine_fed ? 1 : 0;
+      }
+      epilogue_bar();
+      const bool fed = c.ep_ok[0] && c.ep_ok[1] && c.ep_ok[2] && c.ep_ok[3];
+      epilogue_bar();
+      if (!fed) {
+        if (lane == 0 && !mine_fed) flag_error(a.err, ERR_WAIT_EPILOGUE);
+        c.abort = 1;
+        break;
+      }
+      if (t < 0) break;
       const Tile tl = decode_tile<tpair::TOK, WR>(c, G, t);
       if (lane == 0) debug_tile_rows(tl, a);
       const tpair::Shape sh(tl.tile_end - tl.row0, WIDE);
@@ -1039,6 +1173,33 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb0, const C
   return cudaGetLastError();
 }
 
+// Counters of the CTA-pair kernels' tile scheduler: a pair of ints (next tile, clusters
+// finished) per launch slot, zero when the library loads.  Each launch takes the next slot in
+// turn, and the kernel sets its pair back to zero before it completes, so a slot is free again
+// once its launch has finished; launches kTileCtrSlots apart would have to run at the same time
+// to collide.  Part of the library's device image, like the error word: nothing is allocated.
+constexpr int kTileCtrSlots = 256;
+static __device__ int g_tile_ctr[2 * kTileCtrSlots];
+static std::atomic<unsigned> g_tile_ticket{0};
+
+// Device address of this launch's counter pair on the current device (the array's address is
+// looked up once per device, with that device current, under a lock).
+static int* tile_ctr_slot() {
+  static std::mutex mu;
+  static int* base[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_tile_ctr) != cudaSuccess) return nullptr;
+      base[dev] = static_cast<int*>(p);
+    }
+  }
+  return base[dev] + 2 * (g_tile_ticket.fetch_add(1) % kTileCtrSlots);
+}
+
 // Persistent grid of CTA pairs: as many clusters of 2 as can be resident at once (at most
 // half the SMs).  `slot` caches the per-kernel configuration.
 struct PairLaunchCache {
@@ -1084,8 +1245,11 @@ static cudaError_t launch_cluster_pair(Kernel kernel, size_t smem, PairLaunchCac
 
 template <int EPI>
 static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
-                               const GemmArgs& a, cudaStream_t st) {
+                               const GemmArgs& a_in, cudaStream_t st) {
   static PairLaunchCache cache;
+  GemmArgs a = a_in;
+  a.tile_ctr = tile_ctr_slot();
+  if (!a.tile_ctr) return cudaErrorInvalidDevice;
   return launch_cluster_pair(grouped_gemm_pair_kernel<EPI>, pair::SMEM_BYTES, cache, st, ma, mb0, mb1, a);
 }
 
@@ -1093,10 +1257,13 @@ static cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb0, co
 // wide tile); without, that map is the main one and is not used.
 template <int EPI, bool WIDE>
 static cudaError_t launch_tpair(const CUtensorMap& mx, const void* A, long long rows_cap, int K,
-                                const CUtensorMap& mw0, const CUtensorMap& mw1, const GemmArgs& a, cudaStream_t st) {
+                                const CUtensorMap& mw0, const CUtensorMap& mw1, const GemmArgs& a_in, cudaStream_t st) {
   static PairLaunchCache cache;
   CUtensorMap mxt = mx;
   if (WIDE && !make_map_a(&mxt, A, rows_cap, K, tpair::B_TAIL_ROWS)) return cudaErrorInvalidValue;
+  GemmArgs a = a_in;
+  a.tile_ctr = tile_ctr_slot();
+  if (!a.tile_ctr) return cudaErrorInvalidDevice;
   return launch_cluster_pair(grouped_gemm_tpair_kernel<EPI, WIDE>, tpair::Cfg<WIDE>::SMEM_BYTES, cache, st, mx, mxt,
                              mw0, mw1, a);
 }

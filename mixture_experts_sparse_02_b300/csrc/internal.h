@@ -27,6 +27,8 @@ struct GemmArgs {
   uint32_t* err;       // device error word
   unsigned long long wait_limit_ns;  // bound of every pipeline wait
   int starve;          // test hook: the TMA producer issues no copies (the waits run out)
+  int* tile_ctr;       // CTA-pair kernels: [2] ints of their dynamic tile scheduler (next tile,
+                       // clusters finished), zero on entry and reset to zero by the kernel
 };
 
 // Test hook (moe_test_pipeline_fault): arm a starved pipeline with a short wait limit for the
