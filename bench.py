@@ -50,13 +50,12 @@ ORACLE_SAMPLE_TOKENS = {"tiny_f32": 64, "mixtral_prefill": 64, "mixtral_decode":
                         "deepseek_v3": 8}
 FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) per launch of each workload's W1/W2 SwiGLU GEMM, from one ncu
-# capture of a smaller case scaled to the full launch (profiles/): the Mixtral-shaped layer
-# (half the experts and tokens, x 2) and the DeepSeek-V3-shaped one (32 of 256 experts and
-# 1024 of 8192 tokens, x 8).  Valid only for the kernel code it was taken on (gemm_tc.cu
-# without comments, by sha256); null otherwise.
-NCU_TRAFFIC = {"code_sha256": "8d9d90722e723748df0868624429007cb3e672eb7ff4fec1cfd3277912643e93",
-               "bytes_per_launch": {"mixtral_prefill": 2211.0e6, "deepseek_v3": 16718.2e6}}
+# DRAM bytes (read + write) per launch of each workload's W1/W2 SwiGLU GEMM, from one-pass ncu
+# captures (profiles/): the Mixtral- and Hunyuan-shaped launches at full size, the
+# DeepSeek-V3-shaped one on 32 of 256 experts and 1024 of 8192 tokens, x 8.  Valid only for the
+# kernel code it was taken on (gemm_tc.cu without comments, by sha256); null otherwise.
+NCU_TRAFFIC = {"code_sha256": "7c414a0968d2109b8a76485d316ef1ea3fe47f97e69fcf1f0a5184d218295abe",
+               "bytes_per_launch": {"mixtral_prefill": 2176.4e6, "hunyuan_a13b": 4554.1e6, "deepseek_v3": 16490.2e6}}
 
 
 def _code_sha256(path):
@@ -328,8 +327,8 @@ def traffic_for(workload):
 
 def gemm_variant(shape):
     """Which grouped-GEMM kernel the library runs for the routed W1/W2 + SwiGLU GEMM of this
-    workload: the library's rule (CTA pairs when expert blocks average >= 512 rows, the
-    token-wide kernel with wide tiles for 128..511, else single CTAs; f32 layers run on CUDA
+    workload: the library's rule (the token-wide CTA-pair kernel when expert blocks average
+    >= 512 rows, the same with wide tiles for 128..511, else single CTAs; f32 layers run on CUDA
     cores; MOE_GEMM_KERNEL forces one)."""
     if shape.dtype != "bf16":
         return "simt"
@@ -338,7 +337,7 @@ def gemm_variant(shape):
         return forced
     rows = shape.T * shape.k
     if rows >= 512 * shape.E:
-        return "pair"
+        return "tpair"
     return "tpairw" if rows >= 128 * shape.E else "single"
 
 

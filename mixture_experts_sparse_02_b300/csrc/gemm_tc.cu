@@ -1281,10 +1281,16 @@ static void apply_test_hook(GemmArgs& a) {
   }
 }
 
-// Kernel choice, from measurements on B300 (Mixtral-, Hunyuan- and DeepSeek-V3-shaped layers):
-//   expert blocks averaging >= 512 rows: W1/W2 + SwiGLU on the CTA-pair kernel ("pair", 256
-//     token rows per tile), float32 outputs (W3, router logits) on the token-wide CTA-pair kernel
-//     ("tpair", tokens along N in steps of 16);
+// Kernel choice, from measurements on B300 (Mixtral-, Hunyuan- and DeepSeek-V3-shaped layers,
+// both CTA-pair kernels on the dynamic tile schedule):
+//   one dense block (the shared experts, M = T rows): W1/W2 + SwiGLU on the CTA-pair kernel
+//     ("pair", 256 token rows per tile): with no ragged ends it pads nothing and keeps the
+//     tensor pipe busiest (DeepSeek-V3-shaped shared expert 0.55-0.56 ms against 0.58 on the
+//     token-wide kernel); float32 outputs on the token-wide kernel;
+//   expert blocks averaging >= 512 rows: both GEMMs on the token-wide CTA-pair kernel ("tpair",
+//     tokens along N in steps of 16), whose last tile of a block carries at most 15 padding rows
+//     instead of up to 255 (Mixtral-shaped W1/W2 1.25 against 1.27 ms, Hunyuan-shaped
+//     2.29-2.36 against 2.34-2.38 ms);
 //   128..511 rows (DeepSeek-V3 shapes, ~256 rows per expert): both on the token-wide kernel with
 //     wide tiles ("tpairw"): a block of up to 288 rows is one pass over its weight slice;
 //   fewer rows (decode-sized batches): the single-CTA kernel, which streams each expert's
@@ -1295,14 +1301,14 @@ static void apply_test_hook(GemmArgs& a) {
 // the same inputs).
 enum Variant { V_SINGLE = 0, V_PAIR = 1, V_TPAIR = 2, V_TPAIR_WIDE = 3 };
 
-static Variant choose_variant(int epi, long long rows, int groups) {
+static Variant choose_variant(int epi, long long rows, int groups, bool dense) {
   const char* v = getenv("MOE_GEMM_KERNEL");
   if (v && strcmp(v, "single") == 0) return V_SINGLE;
   if (v && strcmp(v, "pair") == 0) return V_PAIR;
   if (v && strcmp(v, "tpair") == 0) return V_TPAIR;
   if (v && strcmp(v, "tpairw") == 0) return V_TPAIR_WIDE;
   const long long g = groups > 0 ? groups : 1;
-  if (rows >= 512LL * g) return epi == EPI_SWIGLU ? V_PAIR : V_TPAIR;
+  if (rows >= 512LL * g) return dense && epi == EPI_SWIGLU ? V_PAIR : V_TPAIR;
   return rows >= 128LL * g ? V_TPAIR_WIDE : V_SINGLE;
 }
 
@@ -1324,7 +1330,7 @@ cudaError_t tc_swiglu(const void* A, long long rows_cap, int K, const void* W1, 
   a.n_tiles = (N + tc::BN / 2 - 1) / (tc::BN / 2);   // 128 output columns per tile (all variants)
   a.b_z = b_z; a.out = h; a.ldo = N; a.accumulate = 0; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
-  switch (tc::choose_variant(EPI_SWIGLU, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
+  switch (tc::choose_variant(EPI_SWIGLU, offsets ? rows_cap : M_dense, offsets ? G : 1, offsets == nullptr)) {
     case tc::V_TPAIR: return tc::launch_tpair<EPI_SWIGLU, false>(ma, A, rows_cap, K, mb0, mb1, a, st);
     case tc::V_TPAIR_WIDE: return tc::launch_tpair<EPI_SWIGLU, true>(ma, A, rows_cap, K, mb0, mb1, a, st);
     case tc::V_PAIR: return tc::launch_pair<EPI_SWIGLU>(ma, mb0, mb1, a, st);
@@ -1343,7 +1349,7 @@ cudaError_t tc_matmul_f32(const void* A, long long rows_cap, int K, const void* 
   a.n_tiles = (N + tc::BN - 1) / tc::BN;             // 256 output columns per tile (all variants)
   a.b_z = b_z; a.out = out; a.ldo = ldo; a.accumulate = accumulate; a.rows_cap = (int)rows_cap; a.err = err;
   tc::apply_test_hook(a);
-  switch (tc::choose_variant(EPI_F32, offsets ? rows_cap : M_dense, offsets ? G : 1)) {
+  switch (tc::choose_variant(EPI_F32, offsets ? rows_cap : M_dense, offsets ? G : 1, offsets == nullptr)) {
     case tc::V_TPAIR: return tc::launch_tpair<EPI_F32, false>(ma, A, rows_cap, K, mb, mb, a, st);
     case tc::V_TPAIR_WIDE: return tc::launch_tpair<EPI_F32, true>(ma, A, rows_cap, K, mb, mb, a, st);
     case tc::V_PAIR: return tc::launch_pair<EPI_F32>(ma, mb, mb, a, st);
