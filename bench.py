@@ -426,10 +426,16 @@ def measure_workload(args, shape, world, rank, pk, headline):
     expert_tflops = (fl_w12 + fl_w3 + fl_sh) / (t_w12 + t_w3 + t_sh) / 1e12
     variant = gemm_variant(shape)
     if shape.dtype == "bf16":
+        traffic = traffic_for(shape.name)
         roof = {"bound": "tensor", "kernel": KERNEL_NAMES[variant] + " (W1/W2 + SiLU*mul)",
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic_for(shape.name),
+                "peak_kind": "bf16 dense burst (%s)" % pk["source"], "traffic": traffic,
                 "traffic_unit": "bytes per launch (dram read + write)", "algorithmic_flops_per_launch": fl_w12}
+        if traffic:
+            # the same launch against the copy bandwidth: the bound at the ridge (DeepSeek-V3 shapes)
+            gbs = traffic / t_w12 / 1e9
+            roof.update({"dram_gbs": round(gbs, 1), "dram_frac": round(gbs / pk["hbm_gbs"], 4),
+                         "dram_peak_gbs": pk["hbm_gbs"]})
         eg = {"tflops": round(expert_tflops, 2), "frac_of_peak": round(expert_tflops / peak, 4), "peak_tflops": peak,
               "w12_ms": round(mean_stage[2], 4), "w3_ms": round(mean_stage[3], 4), "shared_ms": round(mean_stage[4], 4)}
     else:
