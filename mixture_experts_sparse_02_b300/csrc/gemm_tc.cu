@@ -848,6 +848,32 @@ __device__ __forceinline__ void tpair_store_chunk(const GemmArgs& a, const tpair
   if (EPI == EPI_SWIGLU) epilogue_bar();
 }
 
+// The MMA issuer's K loop over one tile of the token-wide kernel: per stage, wait for its data,
+// issue the BK / 16 MMAs (two per K step for a wide tile: the main N = 256 one and the tail one
+// on the same weight stage), and release the stage when they complete.  Returns false if a wait
+// timed out.
+template <bool WIDE_TILE, int STAGE>
+__device__ __forceinline__ bool tpair_mma_kloop(tpair::Ctrl& c, const GemmArgs& a, int num_kb, int& s,
+                                                uint32_t& phase, uint64_t ad_base, uint64_t bd_base, uint32_t d_main,
+                                                uint32_t d_tail, uint32_t idesc_main, uint32_t idesc_tail) {
+  for (int kb = 0; kb < num_kb; ++kb) {
+    if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) return false;
+    tc_fence_after_sync();
+    const uint64_t soff = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
+    const uint64_t ad0 = ad_base + soff, bd0 = bd_base + soff;
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      const uint64_t ad = ad0 + (uint64_t)(kk * (2048 >> 4));
+      const uint64_t bd = bd0 + (uint64_t)(kk * (32 >> 4));
+      umma_bf16_pair(d_main, ad, bd, idesc_main, (kb | kk) != 0);
+      if (WIDE_TILE) umma_bf16_pair(d_tail, ad, bd + (uint64_t)(tpair::B_MAIN >> 4), idesc_tail, (kb | kk) != 0);
+    }
+    umma_commit_pair(&c.empty[s], 0x3);
+    if (++s == tpair::STAGES) { s = 0; phase ^= 1; }
+  }
+  return true;
+}
+
 template <int EPI, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXt,
@@ -983,32 +1009,17 @@ grouped_gemm_tpair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_
         tc_fence_after_sync();
         const uint32_t d_main = tmem + (uint32_t)(buf * BN);
         const uint32_t d_tail = tmem + (uint32_t)((buf ^ 1) * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&c.full[s], phase, &c.abort, a.wait_limit_ns)) { ok = false; break; }
-          tc_fence_after_sync();
-          // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K step
-          // of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.  The
-          // descriptors are the stage-0 ones plus the byte offset / 16 in their address field
-          // (shared addresses stay below 2^18, so the field never carries), and the wide test
-          // stays outside the K-step loop: the issuing thread is on the critical path.
-          const uint64_t soff = (uint64_t)(((uint32_t)s * (uint32_t)STAGE) >> 4);
-          const uint64_t ad0 = ad_base + soff, bd0 = bd_base + soff;
-          if (wide) {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = ad0 + (uint64_t)(kk * (2048 >> 4));
-              const uint64_t bd = bd0 + (uint64_t)(kk * (32 >> 4));
-              umma_bf16_pair(d_main, ad, bd, idesc_main, (kb | kk) != 0);
-              umma_bf16_pair(d_tail, ad, bd + (uint64_t)(tpair::B_MAIN >> 4), idesc_tail, (kb | kk) != 0);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              umma_bf16_pair(d_main, ad0 + (uint64_t)(kk * (2048 >> 4)), bd0 + (uint64_t)(kk * (32 >> 4)), idesc_main,
-                             (kb | kk) != 0);
-          }
-          umma_commit_pair(&c.empty[s], 0x3);
-          if (++s == STAGES) { s = 0; phase ^= 1; }
+        // A: MN-major, two 64-feature blocks B_SUB apart, 8-row k-groups 1024 B apart; a K step
+        // of 16 rows moves 2048 B.  B: K-major token rows of 128 B; a K step moves 32 B.  The
+        // descriptors are the stage-0 ones plus the byte offset / 16 in their address field
+        // (shared addresses stay below 2^18, so the field never carries), and the wide test sits
+        // outside the K loop (one loop per case): the issuing thread is on the critical path.
+        if (WIDE && wide) {
+          ok = tpair_mma_kloop<true, STAGE>(c, a, num_kb, s, phase, ad_base, bd_base, d_main, d_tail, idesc_main,
+                                            idesc_tail);
+        } else {
+          ok = tpair_mma_kloop<false, STAGE>(c, a, num_kb, s, phase, ad_base, bd_base, d_main, d_tail, idesc_main,
+                                             idesc_tail);
         }
         if (!ok) break;
         umma_commit_pair(&c.tfull[buf], 0x3);
