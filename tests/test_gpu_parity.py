@@ -202,6 +202,66 @@ def test_gemm_tile_boundaries(moe, variant, monkeypatch):
     check_close(got, ref, s, "y_perm")
 
 
+def _routed_to(counts, d, seed):
+    """A layer input whose top-1 routing gives expert e exactly counts[e] tokens, in a shuffled
+    token order (so every expert's rows are scattered over x): x is a seeded draw whose first E
+    features are replaced by 4 at the token's expert and 0 elsewhere, and W_g is the identity on
+    those features, so the logits are that one-hot row (a gap of 4 between the first and the
+    second score)."""
+    E = len(counts)
+    owner = np.repeat(np.arange(E), counts)
+    np.random.default_rng(seed).shuffle(owner)
+    T = len(owner)
+    s = S("fwd_tile_boundaries", T=T, d=d, d_ff=320, E=E, k=1, dtype="bf16", scoring="softmax")
+    x = wl.gen_x(s, seed).copy()
+    x[:, :E] = 0
+    x[np.arange(T), owner] = wl.bf16_round(np.float32(4.0))
+    W_g = np.zeros((d, E), dtype=x.dtype)
+    W_g[np.arange(E), np.arange(E)] = wl.bf16_round(np.float32(1.0))
+    return s, x, W_g, owner
+
+
+@pytest.mark.parametrize("variant", ["tpair", "tpairw", "pair", "single"])
+def test_forward_tile_boundaries(moe, variant, monkeypatch):
+    """The whole layer through moe_forward with expert blocks on every tile boundary (the block
+    sizes of test_gemm_tile_boundaries) and each expert's tokens scattered over x: the routing
+    exact, the output against the oracle's layer, and equal bit for bit to the separate route,
+    dispatch, experts and combine calls."""
+    monkeypatch.setenv("MOE_GEMM_KERNEL", variant)
+    s, x, W_g, owner = _routed_to(np.array(TILE_BOUNDARY_COUNTS, dtype=np.int64), 384, 0)
+    assert s.dtype == "bf16" and x.dtype == np.uint16
+    W = upload_experts(s, 0, keep=range(s.E))
+    get_w = host_weight_fn(W["host"], s)
+    ref = orc.forward(wl.to_f64(x, s.dtype), wl.to_f64(W_g, s.dtype), get_w, s.E, s.k, s.scoring)
+    assert np.array_equal(ref["idx"][:, 0], owner)
+    cfg = moe.config_from_shape(s)
+    ws = torch.empty((moe.workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
+    xd, Wgd = to_dev(x, s), to_dev(W_g, s)
+    y = torch.empty((s.T, s.d), dtype=tdtype(s), device="cuda")
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    moe.forward(cfg, xd, Wgd, W["W1"], W["W2"], W["W3"], y, ws, topk_idx_out=idx)
+    assert moe.get_device_error() == 0
+    assert moe.last_launch_count() == _expected_launches(s)
+    assert np.array_equal(idx.cpu().numpy()[:, 0], owner)
+    check_close(y, ref["y"], s)
+    # the same layer through the separate calls (x_perm written by the dispatch)
+    gate = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty((s.E,), dtype=torch.int32, device="cuda")
+    offsets = torch.empty((s.E + 1,), dtype=torch.int32, device="cuda")
+    perm = torch.empty((s.T * s.k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((s.T * s.k, s.d), dtype=tdtype(s), device="cuda")
+    y_perm = torch.empty((s.T * s.k, s.d), dtype=torch.float32, device="cuda")
+    y_sep = torch.empty_like(y)
+    moe.route(cfg, xd, Wgd, idx, gate, ws=ws)
+    moe.dispatch(cfg, idx, xd, counts, offsets, perm, inv, x_perm, ws)
+    moe.experts(cfg, x_perm, offsets, W["W1"], W["W2"], W["W3"], y_perm, ws)
+    moe.combine(cfg, y_perm, inv, gate, y_sep, ws=ws)
+    assert moe.get_device_error() == 0
+    assert np.array_equal(counts.cpu().numpy(), np.array(TILE_BOUNDARY_COUNTS))
+    assert torch.equal(y, y_sep)
+
+
 FULL = ["mixtral_prefill", "mixtral_decode", "hunyuan_a13b", "deepseek_v3"]
 
 
@@ -280,6 +340,13 @@ def test_full_size(moe, name):
                                      get_w("W3", e))
         check_close(y_perm[a:b], ref_rows, s, "y_perm of expert %d (%d rows)" % (e, b - a))
     assert moe.get_device_error() == 0
+    # every element of the forward's output equals that of the separate calls, whose expert
+    # blocks were checked above
+    y_sep = torch.empty_like(y)
+    moe.combine(cfg, y_perm, inv, gate, y_sep, x=din["x"], Ws1=W.get("Ws1"), Ws2=W.get("Ws2"), Ws3=W.get("Ws3"),
+                ws=ws)
+    assert moe.get_device_error() == 0
+    assert torch.equal(y, y_sep), "moe_forward differs from route/dispatch/experts/combine"
 
 
 def test_empty_batch(moe):
