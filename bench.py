@@ -54,8 +54,8 @@ FLUSH_BYTES = 256 << 20
 # captures (profiles/): the Mixtral- and Hunyuan-shaped launches at full size, the
 # DeepSeek-V3-shaped one on 32 of 256 experts and 1024 of 8192 tokens, x 8.  Valid only for the
 # kernel code it was taken on (gemm_tc.cu without comments, by sha256); null otherwise.
-NCU_TRAFFIC = {"code_sha256": "7c414a0968d2109b8a76485d316ef1ea3fe47f97e69fcf1f0a5184d218295abe",
-               "bytes_per_launch": {"mixtral_prefill": 2176.4e6, "hunyuan_a13b": 4554.1e6, "deepseek_v3": 16490.2e6}}
+NCU_TRAFFIC = {"code_sha256": "8ac26bd91cef21c9279872b73237285eb913d2214b4de820921b0004a38f0de4",
+               "bytes_per_launch": {"mixtral_prefill": 2175.9e6, "hunyuan_a13b": 4456.9e6, "deepseek_v3": 16496.8e6}}
 
 
 def _code_sha256(path):
@@ -82,42 +82,107 @@ def peaks():
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """SM clock, power and clock-event reasons while the timed region runs, from two sources: the
+    nvidia-smi query line every 200 ms, and NVML in this process every ~2 ms.  A step of a few
+    milliseconds makes a timed region shorter than nvidia-smi's interval, so most of its samples
+    fall before and after the region (on an idle, fully clocked GPU); the summary takes the NVML
+    samples between mark_start() and mark_end() when there are enough of them."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvmlClocksEventReason*)
+    NVML_REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+                    (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.lines = []
+        self.nvml = []          # (host time, sm MHz, reason bits, power W)
+        self.nvml_max = None
+        self.nvml_error = None
+        self.region = None
+        self._stop = threading.Event()
+        self._nvml_thread = None
+
+    def _device_id(self):
+        """The GPU as nvidia-smi and NVML name it: its UUID (CUDA and NVML number GPUs
+        differently when CUDA_VISIBLE_DEVICES is set), else the CUDA index."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.dev).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.dev)
+
+    def _nvml_loop(self, ident):
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+        except Exception as e:
+            self.nvml_error = "init: %s" % e
+            return
+        try:
+            try:
+                h = nv.nvmlDeviceGetHandleByUUID(ident.encode() if isinstance(ident, str) else ident)
+            except Exception as e:
+                self.nvml_error = "by uuid %s: %s" % (ident, e)
+                h = nv.nvmlDeviceGetHandleByIndex(self.dev)
+            self.nvml_max = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            while not self._stop.is_set():
+                t = time.perf_counter()
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                self.nvml.append((t, float(sm), int(bits), pw))
+                time.sleep(0.002)
+        except Exception as e:
+            self.nvml_error = "sampling: %s" % e
+        finally:
+            try:
+                nv.nvmlShutdown()
+            except Exception:
+                pass
 
     def __enter__(self):
+        ident = self._device_id()
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", ident, "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
-            time.sleep(0.25)
         except (OSError, ValueError):
             self.proc = None
+        self._nvml_thread = threading.Thread(target=self._nvml_loop, args=(ident,), daemon=True)
+        self._nvml_thread.start()
+        time.sleep(0.25)
         return self
+
+    def mark_start(self):
+        self.region = [time.perf_counter(), None]
+
+    def mark_end(self):
+        if self.region:
+            self.region[1] = time.perf_counter()
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        time.sleep(0.25)
+        self._stop.set()
+        if self._nvml_thread is not None:
+            self._nvml_thread.join(timeout=5)
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def _smi_summary(self):
         rows = []
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -139,6 +204,31 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+    def summary(self):
+        smi = self._smi_summary()
+        inside = []
+        if self.region and self.region[1] is not None:
+            inside = [r for r in self.nvml if self.region[0] <= r[0] <= self.region[1]]
+        if len(inside) >= 3:
+            reasons = set(smi["reasons"]) if smi else set()
+            for _, _, bits, _ in inside:
+                for bit, name in self.NVML_REASONS:
+                    if bits & bit:
+                        reasons.add(name)
+            out = {"sm_mhz": statistics.median(r[1] for r in inside),
+                   "sm_mhz_min": min(r[1] for r in inside),
+                   "sm_max_mhz": self.nvml_max or (smi["sm_max_mhz"] if smi else None),
+                   "power_w": round(statistics.median(r[3] for r in inside), 1),
+                   "reasons": sorted(reasons), "source": "NVML every ~2 ms inside the timed region",
+                   "samples": len(inside)}
+            if smi:
+                out["nvidia_smi"] = smi
+            return out
+        if smi:
+            smi["source"] = "nvidia-smi every 200 ms"
+            smi["nvml"] = {"samples": len(self.nvml), "in_region": len(inside), "error": self.nvml_error}
+        return smi
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -392,6 +482,7 @@ def measure_workload(args, shape, world, rank, pk, headline):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
+        clk.mark_start()
         for i in range(args.steps):
             flush.zero_()
             tev[i][0].record()
@@ -399,6 +490,7 @@ def measure_workload(args, shape, world, rank, pk, headline):
             tev[i][1].record()
             launches += moe.last_launch_count()
         torch.cuda.synchronize()
+        clk.mark_end()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in tev]
     # stage split: moe_forward_profiled, the same kernels with events at the stage boundaries
