@@ -115,32 +115,78 @@ class ClockSampler:
         except Exception:
             return str(self.dev)
 
+    @staticmethod
+    def _nvml_api():
+        """The four NVML queries the sampler needs, through the driver's libnvidia-ml (its public
+        C API, called with ctypes), else through the pynvml package."""
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            lib = None
+        if lib is not None:
+            dev_t = ctypes.c_void_p
+
+            def check(r, what):
+                if r != 0:
+                    raise RuntimeError("%s returned %d" % (what, r))
+            check(lib.nvmlInit_v2(), "nvmlInit_v2")
+
+            def handle(ident, index):
+                h = dev_t()
+                if lib.nvmlDeviceGetHandleByUUID(ident.encode(), ctypes.byref(h)) != 0:
+                    check(lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)),
+                          "nvmlDeviceGetHandleByIndex_v2")
+                return h
+
+            def uint_query(fn, h, *args):
+                v = ctypes.c_uint()
+                check(fn(h, *args, ctypes.byref(v)), fn.__name__)
+                return v.value
+
+            def reasons(h):
+                v = ctypes.c_ulonglong()
+                check(lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(v)), "reasons")
+                return v.value
+            return {"handle": handle,
+                    "sm": lambda h: uint_query(lib.nvmlDeviceGetClockInfo, h, ctypes.c_int(1)),
+                    "sm_max": lambda h: uint_query(lib.nvmlDeviceGetMaxClockInfo, h, ctypes.c_int(1)),
+                    "reasons": reasons,
+                    "power_w": lambda h: uint_query(lib.nvmlDeviceGetPowerUsage, h) / 1000.0,
+                    "shutdown": lib.nvmlShutdown}
+        import pynvml as nv
+        nv.nvmlInit()
+
+        def handle(ident, index):
+            try:
+                return nv.nvmlDeviceGetHandleByUUID(ident)
+            except Exception:
+                return nv.nvmlDeviceGetHandleByIndex(index)
+        return {"handle": handle,
+                "sm": lambda h: nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM),
+                "sm_max": lambda h: nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM),
+                "reasons": nv.nvmlDeviceGetCurrentClocksEventReasons,
+                "power_w": lambda h: nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
+                "shutdown": nv.nvmlShutdown}
+
     def _nvml_loop(self, ident):
         try:
-            import pynvml as nv
-            nv.nvmlInit()
+            api = self._nvml_api()
         except Exception as e:
             self.nvml_error = "init: %s" % e
             return
         try:
-            try:
-                h = nv.nvmlDeviceGetHandleByUUID(ident.encode() if isinstance(ident, str) else ident)
-            except Exception as e:
-                self.nvml_error = "by uuid %s: %s" % (ident, e)
-                h = nv.nvmlDeviceGetHandleByIndex(self.dev)
-            self.nvml_max = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            h = api["handle"](ident, self.dev)
+            self.nvml_max = float(api["sm_max"](h))
             while not self._stop.is_set():
                 t = time.perf_counter()
-                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
-                self.nvml.append((t, float(sm), int(bits), pw))
+                self.nvml.append((t, float(api["sm"](h)), int(api["reasons"](h)), api["power_w"](h)))
                 time.sleep(0.002)
         except Exception as e:
             self.nvml_error = "sampling: %s" % e
         finally:
             try:
-                nv.nvmlShutdown()
+                api["shutdown"]()
             except Exception:
                 pass
 
