@@ -54,8 +54,8 @@ FLUSH_BYTES = 256 << 20
 # captures (profiles/): the Mixtral- and Hunyuan-shaped launches at full size, the
 # DeepSeek-V3-shaped one on 32 of 256 experts and 1024 of 8192 tokens, x 8.  Valid only for the
 # kernel code it was taken on (gemm_tc.cu without comments, by sha256); null otherwise.
-NCU_TRAFFIC = {"code_sha256": "8ac26bd91cef21c9279872b73237285eb913d2214b4de820921b0004a38f0de4",
-               "bytes_per_launch": {"mixtral_prefill": 2175.9e6, "hunyuan_a13b": 4456.9e6, "deepseek_v3": 16496.8e6}}
+NCU_TRAFFIC = {"code_sha256": "2574ae6fc36a18dfad5270e6d08b0198df80815f728dbaa1555858fd5f72a499",
+               "bytes_per_launch": {"mixtral_prefill": 2181.8e6, "hunyuan_a13b": 4272.5e6, "deepseek_v3": 16470.4e6}}
 
 
 def _code_sha256(path):
@@ -463,18 +463,15 @@ def traffic_for(workload):
 
 def gemm_variant(shape):
     """Which grouped-GEMM kernel the library runs for the routed W1/W2 + SwiGLU GEMM of this
-    workload: the library's rule (the token-wide CTA-pair kernel when expert blocks average
-    >= 512 rows, the same with wide tiles for 128..511, else single CTAs; f32 layers run on CUDA
-    cores; MOE_GEMM_KERNEL forces one)."""
+    workload: the library's rule (the token-wide CTA-pair kernel with wide tiles when expert
+    blocks average >= 128 rows, else single CTAs; f32 layers run on CUDA cores; MOE_GEMM_KERNEL
+    forces one)."""
     if shape.dtype != "bf16":
         return "simt"
     forced = os.environ.get("MOE_GEMM_KERNEL")
     if forced in ("single", "pair", "tpair", "tpairw"):
         return forced
-    rows = shape.T * shape.k
-    if rows >= 512 * shape.E:
-        return "tpair"
-    return "tpairw" if rows >= 128 * shape.E else "single"
+    return "tpairw" if shape.T * shape.k >= 128 * shape.E else "single"
 
 
 KERNEL_NAMES = {"pair": "grouped_gemm_pair_kernel<EPI_SWIGLU>",

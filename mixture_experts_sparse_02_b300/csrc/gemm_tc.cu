@@ -1298,16 +1298,19 @@ static void apply_test_hook(GemmArgs& a) {
 //     ("pair", 256 token rows per tile): with no ragged ends it pads nothing and keeps the
 //     tensor pipe busiest (DeepSeek-V3-shaped shared expert 0.55-0.56 ms against 0.58 on the
 //     token-wide kernel); float32 outputs on the token-wide kernel;
-//   expert blocks averaging >= 512 rows: both GEMMs on the token-wide CTA-pair kernel ("tpair",
-//     tokens along N in steps of 16), whose last tile of a block carries at most 15 padding rows
-//     instead of up to 255 (Mixtral-shaped W1/W2 1.25 against 1.27 ms, Hunyuan-shaped
-//     2.29-2.36 against 2.34-2.38 ms);
-//   128..511 rows (DeepSeek-V3 shapes, ~256 rows per expert): both on the token-wide kernel with
-//     wide tiles ("tpairw"): a block of up to 288 rows is one pass over its weight slice;
+//   expert blocks averaging >= 128 rows: W1/W2 + SwiGLU on the token-wide CTA-pair kernel with
+//     wide tiles ("tpairw", tokens along N in steps of 16; an expert's last tile may take up to
+//     32 tokens beyond 256 through a second MMA on the same weight stage).  A k-block of a
+//     separate 16..32-token tail tile costs as many cycles as a full one (~530: its weight
+//     stream sets the pace), the second MMA of a wide tile about 250, so the wide build wins on
+//     every block size: Mixtral-shaped W1/W2 1.220-1.224 against 1.241-1.242 ms without wide
+//     tiles, Hunyuan-shaped 2.25-2.29 against 2.28-2.31 ms (one box, three runs each);
+//   W3 (float32 out) on blocks averaging >= 512 rows: the token-wide kernel without wide tiles
+//     ("tpair"; Mixtral-shaped 0.625-0.630 against 0.669-0.676 ms with them), with wide tiles
+//     for 128..511 rows (DeepSeek-V3 shapes, ~256 rows per expert: a block of up to 288 rows is
+//     one pass over its weight slice);
 //   fewer rows (decode-sized batches): the single-CTA kernel, which streams each expert's
 //     weights once with the fewest bytes per row.
-// Without wide tiles the token-wide kernel is the faster one on large blocks (its last tile is
-// then a separate short tile, but there is one per four or more full tiles).
 // MOE_GEMM_KERNEL=single|pair|tpair|tpairw overrides the choice (the tests run every kernel on
 // the same inputs).
 enum Variant { V_SINGLE = 0, V_PAIR = 1, V_TPAIR = 2, V_TPAIR_WIDE = 3 };
@@ -1319,7 +1322,7 @@ static Variant choose_variant(int epi, long long rows, int groups, bool dense) {
   if (v && strcmp(v, "tpair") == 0) return V_TPAIR;
   if (v && strcmp(v, "tpairw") == 0) return V_TPAIR_WIDE;
   const long long g = groups > 0 ? groups : 1;
-  if (rows >= 512LL * g) return dense && epi == EPI_SWIGLU ? V_PAIR : V_TPAIR;
+  if (rows >= 512LL * g) return epi == EPI_SWIGLU ? (dense ? V_PAIR : V_TPAIR_WIDE) : V_TPAIR;
   return rows >= 128LL * g ? V_TPAIR_WIDE : V_SINGLE;
 }
 
