@@ -82,7 +82,7 @@ def peaks():
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """SM clock, power and clock-event reasons while the timed region runs, from two sources: the
+    """SM clock and clock-event reasons while the timed region runs, from two sources: the
     nvidia-smi query line every 200 ms, and NVML in this process every ~2 ms.  A step of a few
     milliseconds makes a timed region shorter than nvidia-smi's interval, so most of its samples
     fall before and after the region (on an idle, fully clocked GPU); the summary takes the NVML
@@ -98,7 +98,7 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.lines = []
-        self.nvml = []          # (host time, sm MHz, reason bits, power W)
+        self.nvml = []          # (host time, sm MHz, reason bits)
         self.nvml_max = None
         self.nvml_error = None
         self.region = None
@@ -117,7 +117,7 @@ class ClockSampler:
 
     @staticmethod
     def _nvml_api():
-        """The four NVML queries the sampler needs, through the driver's libnvidia-ml (its public
+        """The NVML queries the sampler needs, through the driver's libnvidia-ml (its public
         C API, called with ctypes), else through the pynvml package."""
         import ctypes
         try:
@@ -152,7 +152,6 @@ class ClockSampler:
                     "sm": lambda h: uint_query(lib.nvmlDeviceGetClockInfo, h, ctypes.c_int(1)),
                     "sm_max": lambda h: uint_query(lib.nvmlDeviceGetMaxClockInfo, h, ctypes.c_int(1)),
                     "reasons": reasons,
-                    "power_w": lambda h: uint_query(lib.nvmlDeviceGetPowerUsage, h) / 1000.0,
                     "shutdown": lib.nvmlShutdown}
         import pynvml as nv
         nv.nvmlInit()
@@ -166,7 +165,6 @@ class ClockSampler:
                 "sm": lambda h: nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM),
                 "sm_max": lambda h: nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM),
                 "reasons": nv.nvmlDeviceGetCurrentClocksEventReasons,
-                "power_w": lambda h: nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
                 "shutdown": nv.nvmlShutdown}
 
     def _nvml_loop(self, ident):
@@ -180,7 +178,7 @@ class ClockSampler:
             self.nvml_max = float(api["sm_max"](h))
             while not self._stop.is_set():
                 t = time.perf_counter()
-                self.nvml.append((t, float(api["sm"](h)), int(api["reasons"](h)), api["power_w"](h)))
+                self.nvml.append((t, float(api["sm"](h)), int(api["reasons"](h))))
                 time.sleep(0.002)
         except Exception as e:
             self.nvml_error = "sampling: %s" % e
@@ -258,14 +256,13 @@ class ClockSampler:
             inside = [r for r in self.nvml if self.region[0] <= r[0] <= self.region[1]]
         if len(inside) >= 3:
             reasons = set(smi["reasons"]) if smi else set()
-            for _, _, bits, _ in inside:
+            for _, _, bits in inside:
                 for bit, name in self.NVML_REASONS:
                     if bits & bit:
                         reasons.add(name)
             out = {"sm_mhz": statistics.median(r[1] for r in inside),
                    "sm_mhz_min": min(r[1] for r in inside),
                    "sm_max_mhz": self.nvml_max or (smi["sm_max_mhz"] if smi else None),
-                   "power_w": round(statistics.median(r[3] for r in inside), 1),
                    "reasons": sorted(reasons), "source": "NVML every ~2 ms inside the timed region",
                    "samples": len(inside)}
             if smi:
