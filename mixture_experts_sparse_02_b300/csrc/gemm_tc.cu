@@ -16,13 +16,14 @@
 //   grouped_gemm_pair_kernel   a cluster of 2 CTAs shares one tcgen05.mma.cta_group::2 of
 //                              256 token rows x 256 columns; each CTA loads its 128 rows and
 //                              half of the weight columns; 6 x 32 KB stages.  W1/W2 + SwiGLU
-//                              for blocks averaging >= 512 rows.
+//                              of one dense block of >= 512 rows (the shared experts).
 //   grouped_gemm_tpair_kernel  the CTA pair with the roles swapped: weight features along the
 //                              MMA's M (256), tokens along N in steps of 16 up to 256, so the
-//                              last tile of a block carries at most 15 padding rows.  The
-//                              float32-output GEMMs for blocks averaging >= 512 rows; with
+//                              last tile of a block carries at most 15 padding rows.  With
 //                              "wide" tiles (an expert's last tile takes up to 32 more tokens)
-//                              both GEMMs for blocks averaging 128..511 rows.
+//                              W1/W2 + SwiGLU for blocks averaging >= 128 rows and the
+//                              float32-output GEMMs for 128..511; without them the float32
+//                              GEMMs for blocks averaging >= 512 rows.
 // Tiles are walked as (group, column tile, row tile), row tiles fastest, so the CTAs that run
 // at the same time share one weight tile and the weights are streamed from HBM about once.
 // Row tiles may run past the end of their group: the extra rows belong to the next group (or
