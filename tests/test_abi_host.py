@@ -35,6 +35,40 @@ def test_exports_every_declared_symbol(moe):
     assert set(names) == set(moe.EXPORTS)
 
 
+C_CALLER = r"""
+#include <stdio.h>
+#include "moe.h"
+/* A C99 caller: configure a Mixtral-shaped layer, size its workspace, and reference every
+   declared entry point through a function pointer (nothing is called on a device). */
+int main(void) {
+  moe_config c = {4096, 4096, 14336, 8, 2, MOE_BF16, MOE_SOFTMAX_TOPK_RENORM, 0, 0, 0.0f};
+  size_t ws = moe_workspace_bytes(&c);
+  moe_status (*fwd)(const moe_config*, const void*, const void*, const float*, const float*, const void*,
+                    const void*, const void*, const void*, const void*, const void*, void*, int32_t*, int32_t*,
+                    void*, size_t, moe_stream_t) = moe_forward;
+  printf("%zu %s %d %p\n", ws, moe_status_string(MOE_OK), MOE_NUM_STAGES, (void*)fwd);
+  return ws > 0 ? 0 : 1;
+}
+"""
+
+
+def test_header_compiles_and_links_as_c(moe, tmp_path):
+    """include/moe.h is plain C: a C99 program includes it, type-checks a call signature and
+    links against the library (it is not run: the library needs the CUDA driver)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    lib_dir = os.path.dirname(moe.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-o", str(tmp_path / "caller"), "-L", lib_dir, "-l:libmoe.so", "-Wl,--allow-shlib-undefined"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(moe):
     for s in range(6):
         assert moe.status_string(s) and moe.status_string(s) != "unknown status"
