@@ -36,6 +36,10 @@ SMALL = [
     S("f32_e48", T=70, d=40, d_ff=24, E=48, k=5, dtype="f32", scoring="softmax", logit_bias_std=1.0),
     S("bf16_e32_router", T=150, d=320, d_ff=96, E=32, k=4, dtype="bf16", scoring="softmax", logit_bias_std=0.5),
     S("f32_e2", T=90, d=64, d_ff=32, E=2, k=1, dtype="f32", scoring="sigmoid"),
+    # the limits the ABI accepts: E = 1024 experts (the GEMMs' group tables hold exactly that
+    # many) and k = 32 experts per token
+    S("bf16_e1024_limit", T=512, d=128, d_ff=256, E=1024, k=8, dtype="bf16", scoring="softmax"),
+    S("bf16_k32_limit", T=96, d=128, d_ff=128, E=64, k=32, dtype="bf16", scoring="sigmoid"),
 ]
 
 # Shapes for running every grouped-GEMM kernel on the same inputs: 128-row single-CTA tiles,
@@ -51,6 +55,8 @@ GEMM_SHAPES = [
     # 280 rows per shared expert: one wide token tile, accumulated by the second shared expert
     S("gemm_wide_shared", T=280, d=256, d_ff=200, E=8, k=2, dtype="bf16", scoring="softmax",
       n_shared=2, d_ff_shared=72),
+    # 1024 expert groups, most of them a few rows: the largest group table of every kernel
+    S("gemm_e1024", T=512, d=128, d_ff=256, E=1024, k=8, dtype="bf16", scoring="softmax"),
 ]
 
 # Expert block sizes on every boundary of the kernels' row tiles: empty; around the 16-row
