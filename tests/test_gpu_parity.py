@@ -57,6 +57,10 @@ GEMM_SHAPES = [
       n_shared=2, d_ff_shared=72),
     # 1024 expert groups, most of them a few rows: the largest group table of every kernel
     S("gemm_e1024", T=512, d=128, d_ff=256, E=1024, k=8, dtype="bf16", scoring="softmax"),
+    # d = 200: the W1/W2 contraction ends in a partial k-block (8 of 64 columns, the rest
+    # zero-filled by TMA); d_ff = 136: a partial second column tile; blocks of 287..323 rows
+    # (one wide token tile, and full tiles with 33..67-row tails)
+    S("gemm_d200_ktail", T=600, d=200, d_ff=136, E=4, k=2, dtype="bf16", scoring="softmax"),
 ]
 
 # Expert block sizes on every boundary of the kernels' row tiles: empty; around the 16-row
