@@ -659,6 +659,8 @@ def measure_workload(args, shape, world, rank, pk, headline):
            "dtype": shape.dtype, "config": workload_config(shape, world), "roofline": roof, "expert_gemm": eg,
            "decode": decode, "stages_ms": stages,
            "stages_from": "moe_forward_profiled (same kernels, events at the stage boundaries)",
+           "step_ms": {"min": round(min(step_ms), 4), "median": round(statistics.median(step_ms), 4),
+                       "max": round(max(step_ms), 4)},
            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
            "clocks": clk.summary(), "device_error_word": err, "weights_drawn_s": round(gen_s, 1)}
     del W, W_host, x, W_g, lb, ws, y, flush
