@@ -81,6 +81,9 @@ def peaks():
 
 # ----------------------------------------------------------------------------- clocks
 
+IDLE_BEFORE_TIMED_S = 0.25
+
+
 class ClockSampler:
     """SM clock and clock-event reasons while the timed region runs, from two sources: the
     nvidia-smi query line every 200 ms, and NVML in this process every ~2 ms.  A step of a few
@@ -200,7 +203,7 @@ class ClockSampler:
             self.proc = None
         self._nvml_thread = threading.Thread(target=self._nvml_loop, args=(ident,), daemon=True)
         self._nvml_thread.start()
-        time.sleep(0.25)
+        time.sleep(IDLE_BEFORE_TIMED_S)   # both samplers running before the timed region starts
         return self
 
     def mark_start(self):
@@ -516,7 +519,10 @@ def measure_workload(args, shape, world, rank, pk, headline):
         raise RuntimeError("device error word set during warm-up (%s)" % shape.name)
 
     # timed: the production call, moe_forward, bracketed by events on the launching stream (no
-    # events between its kernels, so each may start while the previous one finishes)
+    # events between its kernels, so each may start while the previous one finishes).  The timed
+    # steps start IDLE_BEFORE_TIMED_S after the warm-up steps (the clock sampler's start-up), as
+    # the measured bf16 and copy peaks start from an idle GPU; started right after the warm-ups,
+    # the power cap lengthens the steps of the long layers (recorded in "timing").
     tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
     barrier(world)
@@ -661,6 +667,8 @@ def measure_workload(args, shape, world, rank, pk, headline):
            "stages_from": "moe_forward_profiled (same kernels, events at the stage boundaries)",
            "step_ms": {"min": round(min(step_ms), 4), "median": round(statistics.median(step_ms), 4),
                        "max": round(max(step_ms), 4)},
+           "timing": {"warmup_then_idle_s": IDLE_BEFORE_TIMED_S, "l2": "flushed before every step",
+                      "clock": "CUDA events on the launching stream"},
            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
            "clocks": clk.summary(), "device_error_word": err, "weights_drawn_s": round(gen_s, 1)}
     del W, W_host, x, W_g, lb, ws, y, flush
