@@ -5,7 +5,8 @@
 
 One step = one moe_forward over one batch of T tokens of the workload (route, dispatch,
 grouped SwiGLU experts, shared experts, combine), inputs resident in HBM, L2 flushed (256 MiB
-write) between steps, each step timed with CUDA events on the launching stream.  The stage
+write) between steps, each step timed with CUDA events on the launching stream.  W warm-up
+steps, a 0.25 s pause while the clock samplers start, then K timed steps back to back.  The stage
 split comes from a second pass of moe_forward_profiled (the same kernels with events at the
 stage boundaries, which keep each kernel from starting during its predecessor's tail).  With N > 1 (torchrun, one
 rank per GPU) every rank runs its own batch with replicated weights (the layer is per-token,
