@@ -16,7 +16,9 @@
 //   permute  each warp replays its chunk: a pair's position is its chunk's running position
 //            for that expert plus its rank among the lanes of the same expert in that round.
 //            Pairs of one expert therefore keep ascending i.
-//   gather   x_perm[p] = x[perm_tok[p]], one warp per row with 16-byte vector copies.
+//   scatter  x_perm[inv_pos[t][j]] = x[t], one warp per token: each token row is read once and
+//            written to its k positions (expert-choice routing, which has no inv_pos, gathers
+//            x_perm[p] = x[perm_tok[p]] by row instead).
 // Batches of up to 16384 pairs over at most 256 experts take one single-block kernel for the
 // first three steps instead (dispatch_small_kernel).
 #include "common.cuh"
@@ -200,6 +202,49 @@ __global__ void __launch_bounds__(256) gather_kernel(const V* __restrict__ x, co
   }
 }
 
+// Row scatter, the same x_perm by token: warp t reads token row t once, CH 16-byte vectors per
+// lane at a time, and writes it to the positions of its kept pairs, inv_pos[t][0..k).  A gather
+// by permuted row (above) reads each token's row k times, at scattered times, while the x_perm
+// writes stream through L2 and evict it.
+template <typename V, int CH>
+__global__ void __launch_bounds__(256) scatter_kernel(const V* __restrict__ x, const int32_t* __restrict__ inv_pos,
+                                                      long long T, int k, int vec_per_row, long long rows,
+                                                      V* __restrict__ xp, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long t = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    int p = -1;   // lane j < k: the position of pair (t, j), or -1 (dropped)
+    if (lane < k) {
+      p = __ldg(inv_pos + t * k + lane);
+      const bool in_range = p >= -1 && p < rows;
+      debug_bounds(in_range, err);
+      if (!in_range) p = -1;   // a caller's bad inv_pos (flagged in the bounds-checking build)
+    }
+    const V* src = x + (size_t)t * vec_per_row;
+    // the trip count is the same for every lane (the shuffles below need the whole warp)
+    for (int base = 0; base < vec_per_row; base += 32 * CH) {
+      V buf[CH];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int v = base + 32 * c + lane;
+        if (v < vec_per_row) buf[c] = __ldg(src + v);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int pj = __shfl_sync(FULL, p, j);
+        if (pj < 0) continue;
+        V* dst = xp + (size_t)pj * vec_per_row;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int v = base + 32 * c + lane;
+          if (v < vec_per_row) dst[v] = buf[c];
+        }
+      }
+    }
+  }
+}
+
 // Small batches (T k <= SMALL_PAIRS, E <= SMALL_E), as decode steps produce: the histogram,
 // scan and permutation in one block of 1024 threads, with the same results as the three
 // kernels above, and no atomics either.  Rounds of 1024 pairs in flattened order; warp w of
@@ -347,6 +392,26 @@ cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int c
                                chunk_base, offsets, perm_tok, inv_pos, err));
   g_launches += 3;
   if (launches) *launches += 3;
+  return cudaGetLastError();
+}
+
+cudaError_t scatter_rows(const void* x, long long T, int k, const int32_t* inv_pos, long long rows, int d,
+                         int elem_bytes, void* x_perm, uint32_t* err, cudaStream_t st) {
+  const long long row_bytes = (long long)d * elem_bytes;
+  const int threads = 256;
+  const long long want = (T * 32 + threads - 1) / threads;
+  const unsigned blocks = (unsigned)(want < 148LL * 16 ? want : 148LL * 16);
+  if (row_bytes % 16 == 0 && ((uintptr_t)x % 16 == 0) && ((uintptr_t)x_perm % 16 == 0)) {
+    MOE_RETURN_ON_ERROR(launch_k(scatter_kernel<uint4, 4>, blocks, threads, 0, st, (const uint4*)x, inv_pos, T, k,
+                                 (int)(row_bytes / 16), rows, (uint4*)x_perm, err));
+  } else if (row_bytes % 4 == 0) {
+    MOE_RETURN_ON_ERROR(launch_k(scatter_kernel<uint32_t, 4>, blocks, threads, 0, st, (const uint32_t*)x, inv_pos, T,
+                                 k, (int)(row_bytes / 4), rows, (uint32_t*)x_perm, err));
+  } else {
+    MOE_RETURN_ON_ERROR(launch_k(scatter_kernel<uint16_t, 4>, blocks, threads, 0, st, (const uint16_t*)x, inv_pos, T,
+                                 k, (int)(row_bytes / 2), rows, (uint16_t*)x_perm, err));
+  }
+  ++g_launches;
   return cudaGetLastError();
 }
 

@@ -80,6 +80,9 @@ int dispatch_num_chunks(long long pairs);
 cudaError_t dispatch_indices(const int32_t* topk_idx, int T, int k, int E, int cap, int32_t* chunk_counts,
                              int32_t* chunk_base, int32_t* counts, int32_t* offsets, int32_t* perm_tok,
                              int32_t* inv_pos, uint32_t* err, cudaStream_t st, int* launches);
+// x_perm[inv_pos[t][j]] = x[t] for every kept pair (inv_pos >= 0); rows = the rows of x_perm.
+cudaError_t scatter_rows(const void* x, long long T, int k, const int32_t* inv_pos, long long rows, int d,
+                         int elem_bytes, void* x_perm, uint32_t* err, cudaStream_t st);
 // rows_dev (optional, device): the number of rows to copy, bounded by `rows`.
 cudaError_t gather_rows(const void* x, long long T, const int32_t* perm_tok, long long rows, const int32_t* rows_dev,
                         int d, int elem_bytes, void* x_perm, uint32_t* err, cudaStream_t st);

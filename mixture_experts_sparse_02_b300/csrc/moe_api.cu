@@ -205,7 +205,7 @@ static moe_status stage_dispatch(const moe_config& c, const int32_t* idx, const 
                                  int32_t* chunk_base, cudaStream_t st) {
   MOE_CUDA(dispatch_indices(idx, c.T, c.k, c.E, capacity_slots(c), chunk_counts, chunk_base, counts, offsets, perm,
                             inv, error_word(), st, nullptr));
-  return cuda_status(gather_rows(x, c.T, perm, pairs_of(c), offsets + c.E, c.d, esize(c), x_perm, error_word(), st));
+  return cuda_status(scatter_rows(x, c.T, c.k, inv, pairs_of(c), c.d, esize(c), x_perm, error_word(), st));
 }
 
 static moe_status stage_w12(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* W1,
